@@ -1,0 +1,17 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the package's smoke check and the benchmark's CPU
+baseline leg may import this package.  The product path (the CUDA library
+and its Python binding) never imports, calls or links anything here, and
+nothing here imports the product package.
+"""
+
+from .attention import (  # noqa: F401
+    TILE,
+    allowed_mask,
+    attention_forward,
+    attention_backward,
+    attention_forward_online,
+    attention_forward_rows,
+    live_tiles,
+)

@@ -1,0 +1,233 @@
+"""Plain, slow, fp64 reference for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY: imported by tests, by the package smoke check and
+by the benchmark's CPU-baseline leg, never by the product path.  It shares no
+code with the CUDA library.
+
+What it computes, and where the pages define it:
+
+* Forward (page "FlashAttention", aiwiki, section "Attention and the memory
+  bottleneck", the displayed SDPA formula):
+      S = scale * Q K^T,   P = softmax_row(S + mask),   O = P V
+  Masks "restrict permitted query-key interactions" (same section); here a
+  disallowed pair gets S = -inf before the softmax.
+* Stored row statistic: the per-row log-sum-exp LSE_i = m_i + ln l_i of the
+  scaled, masked scores (page "FlashAttention IO-aware explained", section
+  "Recomputation and IO complexity": compact row statistics (m, l) kept for
+  the backward pass; page "Fast and Memory Efficient Exact Attention",
+  "Summary & Methodology Analysis": the softmax normalisation factor is
+  stored).  LSE is the natural log.
+* Backward: the exact gradient of L = sum(O * dO) with respect to Q, K, V,
+  written out by calculus on the forward formula (the pages defer the
+  closed form to the paper's appendices B.2/B.4, page "FlashAttention: Fast
+  and Memory-Efficient Exact Attention with IO-Awareness", claims on
+  "B.2 Memory-efficient backward pass"):
+      dV = P^T dO
+      dP = dO V^T
+      D_i = sum_c dO_ic O_ic          (= sum_j P_ij dP_ij)
+      dS = P * (dP - D)
+      dQ = scale * dS K,   dK = scale * dS^T Q
+* Online (tiled) forward, used only as a self-check of the two-pass path:
+  the running-max / running-sum / rescaled-accumulator recurrence of page
+  "FlashAttention" (aiwiki), section "Tiling and online normalization":
+      m' = max(m, max s_b)
+      l' = e^{m - m'} l + sum_j e^{s_bj - m'}
+      u' = e^{m - m'} u + sum_j e^{s_bj - m'} v_bj
+      O  = u / l
+* Block-sparse masking: a predefined mask over 128x128 tiles; a pair (i, j)
+  is allowed only if its tile is nonzero (page "Fast and Memory Efficient
+  Exact Attention", "Summary & Methodology Analysis": zero blocks of a
+  predefined block-sparsity mask are skipped).
+
+Readings where the pages are silent (each is listed in the design notes):
+* allowed(b, i, j) = (not causal or j <= i)
+                     and (block_mask is None or block_mask[i//128][j//128] != 0)
+                     and (kv_len is None or j < kv_len[b]).
+* A row with no allowed key has O_i = 0, LSE_i = -inf and contributes no
+  gradient.
+* Inputs are whatever arrays the caller passes (the tests pass the bf16
+  values the GPU receives, upcast to fp64); all arithmetic here is fp64.
+"""
+
+import numpy as np
+
+TILE = 128  # side of one block-mask tile, in queries and in keys
+
+
+def allowed_mask(n, rows=None, causal=False, block_mask=None, kv_len=None,
+                 tile=TILE):
+    """Boolean [len(rows), n]: which (query row, key column) pairs may interact.
+
+    ``kv_len`` is the scalar valid-key count of ONE batch element (or None).
+    """
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    cols = np.arange(n)
+    ok = np.ones((rows.shape[0], n), dtype=bool)
+    if causal:
+        ok &= cols[None, :] <= rows[:, None]
+    if block_mask is not None:
+        bm = np.asarray(block_mask)
+        ok &= bm[rows[:, None] // tile, cols[None, :] // tile] != 0
+    if kv_len is not None:
+        ok &= cols[None, :] < int(kv_len)
+    return ok
+
+
+def _softmax_rows(s, ok):
+    """Two-pass masked softmax of score rows: returns (P, LSE)."""
+    s = np.where(ok, s, -np.inf)
+    m = s.max(axis=1)
+    live = np.isfinite(m)
+    m0 = np.where(live, m, 0.0)
+    e = np.where(ok, np.exp(s - m0[:, None]), 0.0)
+    l = e.sum(axis=1)
+    l1 = np.where(live, l, 1.0)
+    p = e / l1[:, None]
+    lse = np.where(live, m0 + np.log(l1), -np.inf)
+    return p, lse
+
+
+def _as64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _kv(kv_len, b):
+    return None if kv_len is None else int(np.asarray(kv_len)[b])
+
+
+def attention_forward(q, k, v, scale, causal=False, block_mask=None,
+                      kv_len=None, heads=None, row_chunk=1024, tile=TILE):
+    """O [B,H,N,dv] and LSE [B,H,N] by the textbook two-pass definition.
+
+    ``heads`` optionally restricts the work to a list of (b, h) pairs; the
+    other heads of the result are left as NaN.
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, H, N, _ = q.shape
+    o = np.full(v.shape[:3] + (v.shape[3],), np.nan)
+    lse = np.full((B, H, N), np.nan)
+    for b, h in (heads if heads is not None else
+                 [(b, h) for b in range(B) for h in range(H)]):
+        for r0 in range(0, N, row_chunk):
+            rows = np.arange(r0, min(N, r0 + row_chunk))
+            s = scale * (q[b, h, rows] @ k[b, h].T)
+            ok = allowed_mask(N, rows, causal, block_mask, _kv(kv_len, b),
+                              tile)
+            p, lse[b, h, rows] = _softmax_rows(s, ok)
+            o[b, h, rows] = p @ v[b, h]
+    return o, lse
+
+
+def attention_forward_rows(q, k, v, scale, b, h, rows, causal=False,
+                           block_mask=None, kv_len=None, tile=TILE):
+    """O and LSE of selected query rows of one head (sampled full-size checks)."""
+    q, k, v = _as64(q[b, h]), _as64(k[b, h]), _as64(v[b, h])
+    rows = np.asarray(rows)
+    s = scale * (q[rows] @ k.T)
+    ok = allowed_mask(k.shape[0], rows, causal, block_mask, _kv(kv_len, b),
+                      tile)
+    p, lse = _softmax_rows(s, ok)
+    return p @ v, lse
+
+
+def attention_backward(q, k, v, do, scale, causal=False, block_mask=None,
+                       kv_len=None, heads=None, row_chunk=1024, tile=TILE):
+    """dQ, dK, dV [B,H,N,d] of L = sum(O * dO), plus O, LSE and D.
+
+    P is rebuilt here from the inputs (the oracle stores nothing between
+    passes); D uses this function's own fp64 O.  Returns
+    (dq, dk, dv, o, lse, D).
+    """
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    B, H, N, _ = q.shape
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    o = np.full(v.shape, np.nan)
+    lse = np.full((B, H, N), np.nan)
+    dd = np.full((B, H, N), np.nan)
+    for b, h in (heads if heads is not None else
+                 [(b, h) for b in range(B) for h in range(H)]):
+        dk[b, h] = 0.0
+        dv[b, h] = 0.0
+        for r0 in range(0, N, row_chunk):
+            rows = np.arange(r0, min(N, r0 + row_chunk))
+            s = scale * (q[b, h, rows] @ k[b, h].T)
+            ok = allowed_mask(N, rows, causal, block_mask, _kv(kv_len, b),
+                              tile)
+            p, lse[b, h, rows] = _softmax_rows(s, ok)
+            o_r = p @ v[b, h]
+            o[b, h, rows] = o_r
+            d_r = np.sum(do[b, h, rows] * o_r, axis=1)
+            dd[b, h, rows] = d_r
+            dp = do[b, h, rows] @ v[b, h].T
+            ds = p * (dp - d_r[:, None])
+            dq[b, h, rows] = scale * (ds @ k[b, h])
+            dk[b, h] += scale * (ds.T @ q[b, h, rows])
+            dv[b, h] += p.T @ do[b, h, rows]
+    return dq, dk, dv, o, lse, dd
+
+
+def attention_forward_online(q, k, v, scale, causal=False, block_mask=None,
+                             kv_len=None, block_q=128, block_k=128, tile=TILE):
+    """O and LSE by the tiled online-softmax recurrence (self-check path).
+
+    Visits query blocks of ``block_q`` rows and, for each, key blocks of
+    ``block_k`` columns in order, carrying (m, l, u) per row exactly as the
+    recurrence states; never forms a full score row.
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, H, N, _ = q.shape
+    o = np.zeros(v.shape)
+    lse = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, N, block_q):
+                rows = np.arange(r0, min(N, r0 + block_q))
+                m = np.full(rows.shape[0], -np.inf)
+                l = np.zeros(rows.shape[0])
+                u = np.zeros((rows.shape[0], v.shape[3]))
+                for c0 in range(0, N, block_k):
+                    cols = np.arange(c0, min(N, c0 + block_k))
+                    s_b = scale * (q[b, h, rows] @ k[b, h, cols].T)
+                    ok = allowed_mask(N, rows, causal, block_mask,
+                                      _kv(kv_len, b), tile)[:, cols]
+                    s_b = np.where(ok, s_b, -np.inf)
+                    m_new = np.maximum(m, s_b.max(axis=1))
+                    # e^{m - m'}: 0 when nothing was seen yet (m = -inf);
+                    # rows still without an allowed key keep l = 0, u = 0.
+                    fin = np.isfinite(m_new)
+                    ref = np.where(fin, m_new, 0.0)
+                    alpha = np.where(np.isfinite(m), np.exp(m - ref), 0.0)
+                    e = np.where(ok, np.exp(s_b - ref[:, None]), 0.0)
+                    l = alpha * l + e.sum(axis=1)
+                    u = alpha[:, None] * u + e @ v[b, h, cols]
+                    m = m_new
+                live = l > 0
+                o[b, h, rows] = np.where(live[:, None],
+                                         u / np.where(live, l, 1.0)[:, None],
+                                         0.0)
+                lse[b, h, rows] = np.where(
+                    live, m + np.log(np.where(live, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def live_tiles(n, causal=False, block_mask=None, kv_len=None, tile=TILE):
+    """Live (query tile, key tile) pairs of one batch element, by brute force.
+
+    A tile pair is live when at least one of its (i, j) pairs is allowed; it
+    is "partial" when it is live but not every one of its in-range pairs is
+    allowed.  Returns a dict {(qt, kt): partial_flag} -- the enumeration the
+    tiled kernels must visit (tiles with no allowed pair are skipped).
+    """
+    t = (n + tile - 1) // tile
+    ok = allowed_mask(n, None, causal, block_mask, kv_len, tile)
+    out = {}
+    for qt in range(t):
+        r = slice(qt * tile, min(n, (qt + 1) * tile))
+        for kt in range(t):
+            c = slice(kt * tile, min(n, (kt + 1) * tile))
+            blk = ok[r, c]
+            if blk.any():
+                out[(qt, kt)] = int(not blk.all())
+    return out
