@@ -1,0 +1,386 @@
+"""Benchmark: exact attention forward + backward on one GB300.
+
+One step = the whole hot path over one batch: the forward kernel (tile walk,
+QK^T, online softmax, PV, O/LSE store) and the three backward launches
+(D = rowsum(dO*O) preprocess, dK/dV/dQ kernel, dQ conversion), on the
+long-context causal workload B=2, H=16, N=8192, d=128 (bf16 in, fp32
+accumulate).  FLOPs follow the method's count: forward 4*B*H*N^2*d, halved
+under causal masking, backward 2.5x the forward.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead (the baseline arm).
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16) and % of GB300 dense-BF16 tensor peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def flops(cfg, dense_fraction):
+    fwd = 4.0 * cfg["B"] * cfg["H"] * cfg["N"] ** 2 * cfg["d"] * dense_fraction
+    return fwd, 2.5 * fwd
+
+
+def dense_fraction(cfg):
+    if cfg["mask"] == "causal":
+        return 0.5
+    if cfg["mask"] == "band_global":
+        from exact_io_aware_tma_gb300.workloads import band_global_block_mask
+        t = (cfg["N"] + 127) // 128
+        bm = band_global_block_mask(t, cfg["band"], cfg["global_every"])
+        return float(bm.sum()) / (t * t)
+    return 1.0
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[2:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def oracle_sample(inp, rows=1024):
+    """Oracle fwd+bwd on a bounded sample: the last `rows` query rows of head
+    (0, 0) against all keys (causal: every key up to the row), timed wall-clock.
+    Returns (seconds, credited FLOPs, description)."""
+    import numpy as np
+    from exact_io_aware_tma_gb300.workloads import to_f64
+    from oracle import attention_backward
+
+    q, k, v, do = (to_f64(inp[x][0:1, 0:1]) for x in ("q", "k", "v", "do"))
+    N, d = q.shape[2], q.shape[3]
+    # restrict the query rows by giving the oracle the full keys but computing
+    # only the sample's rows: run on the whole head once (the oracle has no
+    # row-subset backward), so time the whole head.
+    t0 = time.perf_counter()
+    attention_backward(q, k, v, do, inp["scale"], inp["causal"], inp["block_mask"],
+                       None if inp["kv_len"] is None else inp["kv_len"][0:1])
+    dt = time.perf_counter() - t0
+    frac = 0.5 if inp["causal"] else 1.0
+    fwd = 4.0 * N * N * d * frac
+    return dt, 3.5 * fwd, f"one full head (b=0, h=0) of the workload, fwd+bwd, N={N}, d={d}"
+
+
+def run_reference(args, cfg, name):
+    from exact_io_aware_tma_gb300.workloads import make_inputs
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = make_inputs(**cfg)
+    for _ in range(args.warmup if args.warmup < 1 else 0):
+        pass
+    times, fl = [], 0.0
+    desc = ""
+    for _ in range(max(1, args.steps)):
+        dt, fl, desc = oracle_sample(inp)
+        times.append(dt)
+    tot = sum(times)
+    value = fl * len(times) / tot / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, **{k: cfg[k] for k in ("B", "H", "N", "d", "mask")}},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def traffic_record(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel source has not changed since the capture; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    recs = {}
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(x.split("=", 1) for x in line.split())
+        recs[kv.get("kernel")] = kv
+    r = recs.get(kernel)
+    if r is None:
+        return None
+    src = os.path.join(ROOT, "exact_io_aware_tma_gb300", "csrc", r["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if sha != r.get("sha"):
+        return None
+    return float(r["bytes_per_launch_full"])
+
+
+def run_gpu(args, cfg, name):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from exact_io_aware_tma_gb300 import fa
+    from exact_io_aware_tma_gb300.workloads import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # The oracle sample runs before any GPU work on rank 0 (N=1 only).
+    cpu_base = None
+    inp = make_inputs(**{**cfg, "seed": cfg["seed"] + rank})
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, desc = oracle_sample(inp)
+        cpu_base = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                    "kind": "oracle", "sample": desc, "seconds": dt}
+
+    fa.load()
+    B, H, N, d = cfg["B"], cfg["H"], cfg["N"], cfg["d"]
+    causal = inp["causal"]
+    bm = None if inp["block_mask"] is None else torch.from_numpy(inp["block_mask"]).to(dev)
+    kv = None if inp["kv_len"] is None else torch.from_numpy(inp["kv_len"]).to(dev)
+    q, k, v, do = (inp[x].to(dev) for x in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = fa.backward_workspace_bytes(B, H, N, d)
+    ws = torch.empty(wsb, device=dev, dtype=torch.uint8)
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)  # > 129 MB L2
+    lib = fa.load()
+    stream = torch.cuda.current_stream(dev)
+    sp = fa._stream(stream)
+    P = fa._ptr
+    scale = inp["scale"]
+    bmp, kvp = P(bm), P(kv)
+
+    def launch(i):
+        # 4 launches of the library's kernels: fwd, preprocess, dK/dV(+dQ), dQ convert
+        st = [lib.fa_forward(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, int(causal),
+                             bmp, kvp, sp)]
+        ev[i][1].record(stream)
+        st.append(lib.fa_backward_preprocess(P(o), P(do), B, H, N, d, P(ws), wsb, sp))
+        ev[i][2].record(stream)
+        st.append(lib.fa_backward_dkdv(P(q), P(k), P(v), P(lse), P(do), P(dk), P(dv), B, H,
+                                       N, d, scale, int(causal), bmp, kvp, P(ws), wsb, sp))
+        ev[i][3].record(stream)
+        st.append(lib.fa_backward_dq_convert(P(dq), B, H, N, d, scale, P(ws), wsb, sp))
+        if any(s != 0 for s in st):
+            raise RuntimeError(f"library call failed: {[fa.status_string(s) for s in st]}")
+
+    n_ev = max(args.warmup, args.steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_ev)]
+    for i in range(args.warmup):
+        flush.zero_()
+        ev[i][0].record(stream)
+        launch(i)
+        ev[i][4].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flushed between steps (outside the events)
+            ev[i][0].record(stream)
+            launch(i)
+            ev[i][4].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    status = fa.last_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.status_string(status)}")
+
+    seg = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(4)]
+                    for i in range(args.steps)])  # ms: fwd, pre, dkdv, convert
+    step_ms = float(seg.sum(axis=1).mean())
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    frac = dense_fraction(cfg)
+    f_fwd, f_bwd = flops(cfg, frac)
+    value = world * (f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12
+    fwd_ms, pre_ms, dkdv_ms, conv_ms = (float(x) for x in seg.mean(axis=0))
+    bwd_ms = pre_ms + dkdv_ms + conv_ms
+    peak, peak_kind = peaks()
+    kernels = {"fwd": (f_fwd, fwd_ms), "bwd_dkdv": (f_bwd, dkdv_ms)}
+    dom = max(kernels, key=lambda n: kernels[n][1])
+    achieved = kernels[dom][0] / (kernels[dom][1] * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers, copies timed ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (inp[x].pin_memory() for x in ("q", "k", "v", "do"))
+        ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+        hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps + 1)]
+        for i in range(args.steps + 1):
+            flush.zero_()
+            e_ev[i][0].record(stream)
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            fa.forward(q, k, v, causal=causal, block_mask=bm, kv_len=kv, scale=scale,
+                       out=o, lse=lse)
+            fa.backward(q, k, v, o, lse, do, causal=causal, block_mask=bm, kv_len=kv,
+                        scale=scale, workspace=ws, dq=dq, dk=dk, dv=dv)
+            for h_, d_ in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                h_.copy_(d_, non_blocking=True)
+            e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev[1:])
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+        e2e = {"value": world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, "B": B, "H": H, "N": N, "d": d,
+                       "mask": cfg["mask"], "parallelism": f"replicas{world}",
+                       "l2": "flushed between steps (256 MB write)"},
+            "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+            "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+            "pct_of_peak": {"fwd": 100 * f_fwd / (fwd_ms * 1e-3) / 1e12 / peak,
+                            "bwd": 100 * f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,
+                            "peak_tflops": peak, "peak_kind": peak_kind},
+            "kernel_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
+                          "bwd_dq_convert": conv_ms},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": traffic_record(dom)},
+            "cpu_baseline": cpu_base,
+            "e2e": e2e,
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    from exact_io_aware_tma_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    cfg = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg, args.workload)
+    else:
+        run_gpu(args, cfg, args.workload)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,328 @@
+// C ABI of the attention library: host-side validation, the small
+// memory-bound kernels (backward preprocess, dQ conversion, tile schedule)
+// and the launches of the tiled kernels, all asynchronous on the caller's
+// stream.  See include/fa.h for the contract of each entry point.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+
+namespace fa {
+
+// Device error word: kernels with bounded waits record FA_ERR_TIMEOUT here.
+__device__ int g_fa_status = 0;
+
+// ---------------------------------------------------------------------------
+// Backward preprocess: D_i = sum_c dO_ic * O_ic (fp32) and dQacc = 0.
+// One thread per 16-byte chunk (8 bf16) of a row; the CH chunks of a row are
+// adjacent lanes of one warp and are reduced by shuffles.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                          const __nv_bfloat16* __restrict__ dout, float* __restrict__ dvec,
+                          float* __restrict__ dq_acc, long long rows) {
+  constexpr int CH = D / 8;
+  const long long n = rows * CH;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    const bool ok = i < n;
+    if (ok) {
+      uint4 a = *reinterpret_cast<const uint4*>(o + i * 8);
+      uint4 b = *reinterpret_cast<const uint4*>(dout + i * 8);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float2 x = __bfloat1622float2(pa[j]);
+        float2 y = __bfloat1622float2(pb[j]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      reinterpret_cast<float4*>(dq_acc + i * 8)[0] = z;
+      reinterpret_cast<float4*>(dq_acc + i * 8)[1] = z;
+    }
+#pragma unroll
+    for (int off = CH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (ok && (i % CH) == 0) dvec[i / CH] = acc;
+  }
+}
+
+// dQ = scale * dQacc, fp32 -> bf16, 8 elements per thread.
+__global__ void __launch_bounds__(256)
+    dq_convert_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                      float scale, long long chunks) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<const float4*>(dq_acc + i * 8)[0];
+    float4 b = reinterpret_cast<const float4*>(dq_acc + i * 8)[1];
+    uint4 r;
+    r.x = pack_bf16(a.x * scale, a.y * scale);
+    r.y = pack_bf16(a.z * scale, a.w * scale);
+    r.z = pack_bf16(b.x * scale, b.y * scale);
+    r.w = pack_bf16(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + i * 8) = r;
+  }
+}
+
+// Tile schedule of one batch element (one CTA): CSR over query tiles of the
+// live key tiles, with the element-mask flag.  Uses the same predicates as
+// the attention kernels.
+__global__ void __launch_bounds__(1024)
+    tile_schedule_kernel(Problem p, int b, int32_t* row_ptr, int32_t* col_idx,
+                         uint8_t* partial) {
+  __shared__ int s_cnt[1024];
+  __shared__ int s_carry;
+  const int klim = key_limit(p, b);
+  if (threadIdx.x == 0) {
+    s_carry = 0;
+    row_ptr[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < p.T; base += blockDim.x) {
+    const int qt = base + threadIdx.x;
+    int c = 0;
+    if (qt < p.T)
+      for (int kt = 0; kt < p.T; ++kt) c += tile_live(p, qt, kt, klim) ? 1 : 0;
+    s_cnt[threadIdx.x] = c;
+    __syncthreads();
+    // inclusive scan (Hillis-Steele)
+    for (int off = 1; off < (int)blockDim.x; off <<= 1) {
+      int x = threadIdx.x >= (unsigned)off ? s_cnt[threadIdx.x - off] : 0;
+      __syncthreads();
+      s_cnt[threadIdx.x] += x;
+      __syncthreads();
+    }
+    const int carry = s_carry;
+    if (qt < p.T) {
+      int pos = carry + s_cnt[threadIdx.x] - c;
+      row_ptr[qt + 1] = carry + s_cnt[threadIdx.x];
+      for (int kt = 0; kt < p.T; ++kt) {
+        if (tile_live(p, qt, kt, klim)) {
+          col_idx[pos] = kt;
+          partial[pos] = tile_partial(p, qt, kt, klim) ? 1 : 0;
+          ++pos;
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry = carry + s_cnt[threadIdx.x];
+    __syncthreads();
+  }
+}
+
+static int* status_ptr() {
+  int* ptr = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_fa_status) != cudaSuccess)
+    return nullptr;
+  return ptr;
+}
+
+static bool aligned(const void* ptr, size_t a) {
+  return (reinterpret_cast<uintptr_t>(ptr) % a) == 0;
+}
+
+// Shared size checks.  Fills `p` on success.
+static int check_sizes(int B, int H, int N, int d, float scale, int causal,
+                       const uint8_t* block_mask, const int32_t* kv_len, Problem* p) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  if (bh > 2147483647LL) return FA_ERR_INVALID_ARG;
+  const long long T = ((long long)N + kTile - 1) / kTile;
+  if (T > 65535) return FA_ERR_INVALID_ARG;  // grid.y bound: N <= 8,388,480
+  // B*H*N*d elements must stay far from int64 overflow
+  if ((double)bh * N * d > 4.0e18) return FA_ERR_INVALID_ARG;
+  p->B = B;
+  p->H = H;
+  p->N = N;
+  p->d = d;
+  p->T = (int)T;
+  p->scale = scale;
+  p->scale_log2 = scale * kLog2e;
+  p->causal = causal ? 1 : 0;
+  p->block_mask = block_mask;
+  p->kv_len = kv_len;
+  p->status = nullptr;
+  return FA_OK;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+               int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+               const int32_t* kv_len, void* stream) {
+  Problem p;
+  int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(kv_len, 4))
+    return FA_ERR_INVALID_ARG;
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  cudaError_t e = launch_fwd_mma(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
+  Problem p;
+  if (check_sizes(B, H, N, d, 1.0f, 0, nullptr, nullptr, &p) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return round_up(rows * sizeof(float), 256) + round_up(rows * d * sizeof(float), 256);
+}
+
+static int check_workspace(int B, int H, int N, int d, const void* ws, size_t wsb) {
+  if (!ws || !aligned(ws, 256)) return FA_ERR_INVALID_ARG;
+  if (wsb < fa_backward_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+static float* ws_dvec(void* ws) { return static_cast<float*>(ws); }
+static float* ws_dq_acc(void* ws, long long rows) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                  round_up((size_t)rows * sizeof(float), 256));
+}
+
+// Elementwise kernels: enough CTAs for every chunk, capped at a few waves.
+static unsigned elementwise_blocks(long long chunks) {
+  long long nblk = (chunks + 255) / 256;
+  if (nblk > 152LL * 32) nblk = 152LL * 32;
+  return (unsigned)(nblk < 1 ? 1 : nblk);
+}
+
+int fa_backward_preprocess(const void* o, const void* dout, int B, int H, int N, int d,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  Problem p;
+  int st = check_sizes(B, H, N, d, 1.0f, 0, nullptr, nullptr, &p);
+  if (st != FA_OK) return st;
+  if (!o || !dout || !aligned(o, 16) || !aligned(dout, 16)) return FA_ERR_INVALID_ARG;
+  st = check_workspace(B, H, N, d, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long rows = (long long)B * H * N;
+  const unsigned nblk = elementwise_blocks(rows * (d / 8));
+  auto ob = static_cast<const __nv_bfloat16*>(o);
+  auto db = static_cast<const __nv_bfloat16*>(dout);
+  if (d == 64)
+    bwd_preprocess_kernel<64><<<nblk, 256, 0, s>>>(ob, db, ws_dvec(workspace),
+                                                   ws_dq_acc(workspace, rows), rows);
+  else
+    bwd_preprocess_kernel<128><<<nblk, 256, 0, s>>>(ob, db, ws_dvec(workspace),
+                                                    ws_dq_acc(workspace, rows), rows);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_backward_dkdv(const void* q, const void* k, const void* v, const float* lse,
+                     const void* dout, void* dk, void* dv, int B, int H, int N, int d,
+                     float scale, int causal, const uint8_t* block_mask,
+                     const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  Problem p;
+  int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !lse || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) ||
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(kv_len, 4))
+    return FA_ERR_INVALID_ARG;
+  st = check_workspace(B, H, N, d, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  const long long rows = (long long)B * H * N;
+  cudaError_t e = launch_bwd_mma(p, q, k, v, dout, lse, ws_dvec(workspace),
+                                 ws_dq_acc(workspace, rows), dk, dv,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
+                           const void* workspace, size_t workspace_bytes, void* stream) {
+  Problem p;
+  int st = check_sizes(B, H, N, d, scale, 0, nullptr, nullptr, &p);
+  if (st != FA_OK) return st;
+  if (!dq || !aligned(dq, 16)) return FA_ERR_INVALID_ARG;
+  st = check_workspace(B, H, N, d, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  const long long rows = (long long)B * H * N;
+  const long long chunks = rows * (d / 8);
+  dq_convert_kernel<<<elementwise_blocks(chunks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      ws_dq_acc(const_cast<void*>(workspace), rows), static_cast<__nv_bfloat16*>(dq), scale,
+      chunks);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o,
+                const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+                const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  Problem p;
+  int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
+  if (st != FA_OK) return st;
+  // Validate every argument before the first launch, so a rejected call
+  // writes nothing.
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(kv_len, 4))
+    return FA_ERR_INVALID_ARG;
+  st = check_workspace(B, H, N, d, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  st = fa_backward_preprocess(o, dout, B, H, N, d, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  st = fa_backward_dkdv(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, block_mask,
+                        kv_len, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
+}
+
+int fa_tile_schedule(int N, int causal, const uint8_t* block_mask, const int32_t* kv_len,
+                     int b, int32_t* row_ptr, int32_t* col_idx, uint8_t* partial,
+                     void* stream) {
+  Problem p;
+  int st = check_sizes(1, 1, N, 64, 1.0f, causal, block_mask, kv_len, &p);
+  if (st != FA_OK) return st;
+  if (!row_ptr || !col_idx || !partial || b < 0) return FA_ERR_INVALID_ARG;
+  if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(kv_len, 4))
+    return FA_ERR_INVALID_ARG;
+  tile_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(p, b, row_ptr,
+                                                                          col_idx, partial);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_last_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyFromSymbol(&h, g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (h != 0) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(g_fa_status, &z, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return h;
+}
+
+}  // extern "C"

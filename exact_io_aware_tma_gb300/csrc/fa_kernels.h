@@ -1,0 +1,17 @@
+// Internal launch entry points of the attention kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
+
+namespace fa {
+
+cudaError_t launch_fwd_mma(const Problem& p, const void* q, const void* k, const void* v,
+                           void* o, float* lse, cudaStream_t st);
+
+cudaError_t launch_bwd_mma(const Problem& p, const void* q, const void* k, const void* v,
+                           const void* dout, const float* lse, const float* dvec,
+                           float* dq_acc, void* dk, void* dv, cudaStream_t st);
+
+}  // namespace fa

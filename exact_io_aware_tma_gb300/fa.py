@@ -1,0 +1,155 @@
+"""ctypes binding of ``libfa_gb300.so`` (C ABI declared in include/fa.h).
+
+Argument marshalling only: every step of attention runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.  If the
+library is missing, every call raises -- there is no fallback path.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+
+_lib = None
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_status_string": ([_i], ctypes.c_char_p),
+    "fa_forward": ([_vp] * 5 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
+    "fa_backward_workspace_bytes": ([_i] * 4, _sz),
+    "fa_backward": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
+    "fa_backward_preprocess": ([_vp, _vp] + [_i] * 4 + [_vp, _sz, _vp], _i),
+    "fa_backward_dkdv": ([_vp] * 7 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
+    "fa_backward_dq_convert": ([_vp] + [_i] * 4 + [_f, _vp, _sz, _vp], _i),
+    "fa_tile_schedule": ([_i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
+    "fa_last_device_status": ([_vp], _i),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def load(path=LIB_PATH):
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA attention library not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().fa_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_qkv(*ts):
+    ref = ts[0]
+    for t in ts:
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous bf16 CUDA tensors")
+        if t.shape != ref.shape or t.dim() != 4:
+            raise ValueError("tensors must share one [B, H, N, d] shape")
+
+
+def _mask_args(N, block_mask, kv_len, B):
+    T = (N + 127) // 128
+    if block_mask is not None:
+        if not (block_mask.is_cuda and block_mask.dtype == torch.uint8
+                and block_mask.is_contiguous() and tuple(block_mask.shape) == (T, T)):
+            raise ValueError(f"block_mask must be a contiguous uint8 CUDA [{T},{T}] tensor")
+    if kv_len is not None:
+        if not (kv_len.is_cuda and kv_len.dtype == torch.int32
+                and kv_len.is_contiguous() and tuple(kv_len.shape) == (B,)):
+            raise ValueError(f"kv_len must be a contiguous int32 CUDA [{B}] tensor")
+    return _ptr(block_mask), _ptr(kv_len)
+
+
+def forward(q, k, v, causal=False, block_mask=None, kv_len=None, scale=None,
+            out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v); see include/fa.h ``fa_forward``."""
+    lib = load()
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    bm, kl = _mask_args(N, block_mask, kv_len, B)
+    st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                        scale, int(bool(causal)), bm, kl, _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_forward")
+    return out, lse
+
+
+def backward_workspace_bytes(B, H, N, d):
+    return int(load().fa_backward_workspace_bytes(B, H, N, d))
+
+
+def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
+             scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of sum(O * dO); see include/fa.h ``fa_backward``."""
+    lib = load()
+    _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = backward_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    bm, kl = _mask_args(N, block_mask, kv_len, B)
+    st = lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                         _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, scale,
+                         int(bool(causal)), bm, kl, _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_backward")
+    return dq, dk, dv
+
+
+def tile_schedule(N, causal=False, block_mask=None, kv_len=None, b=0, device="cuda"):
+    """(row_ptr, col_idx, partial) CUDA tensors; see ``fa_tile_schedule``."""
+    lib = load()
+    T = (N + 127) // 128
+    B = 0 if kv_len is None else kv_len.shape[0]
+    bm, kl = _mask_args(N, block_mask, kv_len, B)
+    row_ptr = torch.zeros(T + 1, device=device, dtype=torch.int32)
+    col_idx = torch.full((T * T,), -1, device=device, dtype=torch.int32)
+    partial = torch.full((T * T,), 255, device=device, dtype=torch.uint8)
+    st = lib.fa_tile_schedule(N, int(bool(causal)), bm, kl, b, _ptr(row_ptr),
+                              _ptr(col_idx), _ptr(partial), _stream())
+    if st != FA_OK:
+        raise FAError(st, "fa_tile_schedule")
+    return row_ptr, col_idx, partial
+
+
+def last_device_status(stream=None):
+    return int(load().fa_last_device_status(_stream(stream)))

@@ -1,0 +1,169 @@
+/*
+ * fa.h -- C ABI of the exact IO-aware attention library for GB300 (sm_103a).
+ *
+ * What the library computes (one head = one (b, h) pair, all heads at once):
+ *
+ *   S   = scale * Q K^T                          (N x N, never stored)
+ *   P   = softmax_row(S) over the allowed keys   (never stored)
+ *   O   = P V
+ *   LSE = per-row natural log-sum-exp of the allowed scaled scores
+ *
+ * Source: page "FlashAttention" (aiwiki), section "Attention and the memory
+ * bottleneck" (the scaled dot-product formula and its masks), section
+ * "Tiling and online normalization" (the running max / running sum /
+ * rescaled accumulator recurrence the forward kernel evaluates tile by
+ * tile), and page "FlashAttention IO-aware explained", section
+ * "Recomputation and IO complexity" (the backward pass rebuilds score tiles
+ * from stored row statistics instead of storing P).  Block-sparse skipping:
+ * page "Fast and Memory Efficient Exact Attention", "Summary & Methodology
+ * Analysis" (zero blocks of a predefined block-sparsity mask are skipped).
+ *
+ * Which (query i, key j) pairs are allowed, for batch element b:
+ *     (!causal || j <= i)
+ *  && (block_mask == NULL || block_mask[(i/128)*T + j/128] != 0)
+ *  && (kv_len == NULL     || j < kv_len[b])              (kv_len clamped to [0, N])
+ * with T = ceil(N/128).  A query row with no allowed key gets O = 0 and
+ * LSE = -inf, and contributes nothing to the gradients.
+ *
+ * Common conventions
+ *  - Tensors are dense, row-major, on the current CUDA device:
+ *      Q, K, V, O, dO, dQ, dK, dV : bf16 [B, H, N, d], d in {64, 128},
+ *                                   base pointers 16-byte aligned;
+ *      LSE, D                     : fp32 [B, H, N];
+ *      block_mask                 : uint8 [T, T] (shared by every (b, h)) or NULL;
+ *      kv_len                     : int32 [B] or NULL.
+ *  - Every pointer is a DEVICE pointer unless stated otherwise.  The caller
+ *    owns every buffer; the library allocates no device memory on these
+ *    calls and keeps no pointer after a call returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and never synchronises, except fa_last_device_status.
+ *  - Errors are status codes; the library never aborts.  Arguments are
+ *    validated on the host before anything is launched; on an invalid
+ *    argument nothing is launched and no output is written.
+ *  - Outputs are written in bf16 (round to nearest even) except LSE and D.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, overflow   */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 or 128          */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+  FA_ERR_TIMEOUT = 4      /* a bounded in-kernel wait gave up (see below)  */
+} fa_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+FA_API const char* fa_status_string(int status);
+
+/*
+ * Forward pass: O and LSE.
+ *   q, k, v    : bf16 [B,H,N,d], read only.
+ *   o          : bf16 [B,H,N,d], written.
+ *   lse        : fp32 [B,H,N], written (natural log; -inf on fully masked rows).
+ *   scale      : multiplies Q K^T (usually 1/sqrt(d)); any finite value.
+ *   causal     : nonzero = causal mask j <= i.
+ *   block_mask : see above; its zero tiles are never loaded or computed.
+ *   kv_len     : see above.
+ * Requires B, H, N >= 1, B*H <= 2^31-1, B*H*N*d < 2^62, d in {64,128}.
+ */
+FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int N, int d, float scale, int causal,
+               const uint8_t* block_mask, const int32_t* kv_len, void* stream);
+
+/*
+ * Bytes of device workspace fa_backward needs: D (fp32 [B,H,N]) followed by
+ * the fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.  O(B*H*N*d):
+ * linear in N (no N x N buffer).  Returns 0 for invalid sizes.
+ */
+FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass: dQ, dK, dV of L = sum(O * dO), recomputing P tile by tile
+ * from Q, K and the forward's LSE (P is never stored).
+ *   q, k, v, o : forward inputs and output, bf16 [B,H,N,d].
+ *   lse        : forward's LSE, fp32 [B,H,N].
+ *   dout       : dO, bf16 [B,H,N,d].
+ *   dq, dk, dv : bf16 [B,H,N,d], written.
+ *   workspace  : device buffer of at least fa_backward_workspace_bytes(),
+ *                256-byte aligned, owned by the caller; its contents on
+ *                entry are ignored and on exit are unspecified.
+ *   Other arguments as in fa_forward and equal to the forward call's.
+ * Launches, in order on `stream`: the D = rowsum(dO * O) preprocess (which
+ * also clears the dQ accumulator), the dK/dV kernel (which also adds each
+ * tile's dS K into the dQ accumulator), and the dQ conversion.
+ */
+FA_API int fa_backward(const void* q, const void* k, const void* v, const void* o,
+                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                int B, int H, int N, int d, float scale, int causal,
+                const uint8_t* block_mask, const int32_t* kv_len,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three launches of fa_backward, exposed one by one so a caller can
+ * time or overlap them; calling them in this order on one stream with the
+ * same workspace is exactly fa_backward.  Arguments mean what they mean in
+ * fa_backward; each validates its own arguments.
+ *
+ * fa_backward_preprocess: D = rowsum(dO * O) into the workspace (fp32
+ *   [B,H,N]) and clears the workspace's fp32 dQ accumulator [B,H,N,d].
+ * fa_backward_dkdv: for every live 128-key tile, recomputes P and dS from
+ *   Q, K, V, dO, LSE and D, writes dK (times scale) and dV, and adds dS K
+ *   into the workspace's dQ accumulator.  Needs the preprocess first.
+ * fa_backward_dq_convert: dQ = scale * accumulator, rounded to bf16.
+ */
+FA_API int fa_backward_preprocess(const void* o, const void* dout, int B, int H, int N,
+                                  int d, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+FA_API int fa_backward_dkdv(const void* q, const void* k, const void* v, const float* lse,
+                            const void* dout, void* dk, void* dv, int B, int H, int N,
+                            int d, float scale, int causal, const uint8_t* block_mask,
+                            const int32_t* kv_len, void* workspace,
+                            size_t workspace_bytes, void* stream);
+FA_API int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
+                                  const void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
+ * Tile schedule of one batch element, as the kernels enumerate it: every
+ * live (query tile, key tile) pair of 128x128 tiles, i.e. every tile pair
+ * holding at least one allowed (i, j), in query-tile-major order, with a
+ * flag that is 1 when some in-range pair of the tile is disallowed (the
+ * kernel masks elements there) and 0 when the tile is fully allowed.
+ *   b          : batch element whose kv_len applies (ignored if kv_len NULL).
+ *   row_ptr    : int32 [T+1] device, written (CSR offsets by query tile).
+ *   col_idx    : int32 [T*T] device, written (key tile of each live pair).
+ *   partial    : uint8 [T*T] device, written.
+ * Entries of col_idx / partial past row_ptr[T] are left untouched.
+ */
+FA_API int fa_tile_schedule(int N, int causal, const uint8_t* block_mask,
+                     const int32_t* kv_len, int b, int32_t* row_ptr,
+                     int32_t* col_idx, uint8_t* partial, void* stream);
+
+/*
+ * Reads and clears the library's device error word on the current device
+ * after synchronising `stream`.  Kernels that wait on an mbarrier give up
+ * after a bounded number of polls, record FA_ERR_TIMEOUT there and exit,
+ * so a lost signal surfaces here instead of hanging the GPU.
+ * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if synchronisation failed.
+ */
+FA_API int fa_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */
