@@ -116,26 +116,33 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle arm
 
-def oracle_sample(inp, rows=1024):
-    """Oracle fwd+bwd on a bounded sample: the last `rows` query rows of head
-    (0, 0) against all keys (causal: every key up to the row), timed wall-clock.
-    Returns (seconds, credited FLOPs, description)."""
-    import numpy as np
+def oracle_sample(inp, budget_s=10.0):
+    """Oracle fwd+bwd on a bounded sample of the workload: whole heads, taken in
+    order (0,0), (0,1), ... until `budget_s` seconds of CPU work have been spent
+    (at least one head).  Returns (seconds, credited FLOPs, description)."""
     from exact_io_aware_tma_gb300.workloads import to_f64
     from oracle import attention_backward
 
-    q, k, v, do = (to_f64(inp[x][0:1, 0:1]) for x in ("q", "k", "v", "do"))
-    N, d = q.shape[2], q.shape[3]
-    # restrict the query rows by giving the oracle the full keys but computing
-    # only the sample's rows: run on the whole head once (the oracle has no
-    # row-subset backward), so time the whole head.
-    t0 = time.perf_counter()
-    attention_backward(q, k, v, do, inp["scale"], inp["causal"], inp["block_mask"],
-                       None if inp["kv_len"] is None else inp["kv_len"][0:1])
-    dt = time.perf_counter() - t0
+    B, H, N, d = inp["q"].shape
     frac = 0.5 if inp["causal"] else 1.0
-    fwd = 4.0 * N * N * d * frac
-    return dt, 3.5 * fwd, f"one full head (b=0, h=0) of the workload, fwd+bwd, N={N}, d={d}"
+    if inp["block_mask"] is not None:
+        frac = float(inp["block_mask"].sum()) / inp["block_mask"].size
+    per_head = 3.5 * 4.0 * N * N * d * frac  # fwd + 2.5x fwd, the method's count
+    heads, spent = 0, 0.0
+    for b in range(B):
+        for h in range(H):
+            q, k, v, do = (to_f64(inp[x][b:b + 1, h:h + 1]) for x in ("q", "k", "v", "do"))
+            kv = None if inp["kv_len"] is None else inp["kv_len"][b:b + 1]
+            t0 = time.perf_counter()
+            attention_backward(q, k, v, do, inp["scale"], inp["causal"], inp["block_mask"], kv)
+            spent += time.perf_counter() - t0
+            heads += 1
+            if spent >= budget_s:
+                break
+        if spent >= budget_s:
+            break
+    return spent, heads * per_head, (f"{heads} whole head(s) of the workload, fwd+bwd "
+                                     f"(fp64 numpy, BLAS threads = all cores), N={N}, d={d}")
 
 
 def run_reference(args, cfg, name):
@@ -144,8 +151,6 @@ def run_reference(args, cfg, name):
     if rank != 0:
         return
     inp = make_inputs(**cfg)
-    for _ in range(args.warmup if args.warmup < 1 else 0):
-        pass
     times, fl = [], 0.0
     desc = ""
     for _ in range(max(1, args.steps)):

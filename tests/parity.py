@@ -7,6 +7,12 @@ inputs, fp32 accumulation):
   dQ, dK, dV  : max |gpu - ref| <= 2e-2 * max |ref|
   LSE         : max |gpu - ref| <= 1e-3 on rows with an allowed key;
                 exactly -inf (and O == 0) on rows without one.
+
+When a reference tensor is identically zero (e.g. dQ with a single key,
+where dS = P (dP - D) vanishes), the relative bound has nothing to scale;
+the bound then uses max |ref| floored at ABS_FLOOR = 1e-4 (inputs are
+N(0, 1), so 1e-4 sits far below every nonzero reference magnitude in the
+tests and far above the fp32 rounding noise such a zero picks up).
 """
 
 import numpy as np
@@ -16,6 +22,7 @@ from exact_io_aware_tma_gb300 import fa
 from exact_io_aware_tma_gb300.workloads import to_f64
 
 TOL_O, TOL_GRAD, TOL_LSE = 1e-2, 2e-2, 1e-3
+ABS_FLOOR = 1e-4
 
 
 def to_device(inp, dev="cuda"):
@@ -49,10 +56,10 @@ def oracle_inputs(inp):
 def check_close(name, got, want, tol):
     assert got.shape == want.shape, (name, got.shape, want.shape)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
-    ref = np.abs(want).max()
+    ref = max(np.abs(want).max(), ABS_FLOOR)
     err = np.abs(got - want).max()
-    assert err <= tol * max(ref, 1e-30), f"{name}: max err {err:.3e} > {tol} * {ref:.3e}"
-    return err / max(ref, 1e-30)
+    assert err <= tol * ref, f"{name}: max err {err:.3e} > {tol} * {ref:.3e}"
+    return err / ref
 
 
 def check_lse(got, want):
