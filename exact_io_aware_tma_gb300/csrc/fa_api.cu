@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-static int* status_ptr() {
+int* status_word() {
   int* ptr = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_fa_status) != cudaSuccess)
     return nullptr;
@@ -181,9 +181,9 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || !aligned(kv_len, 4))
     return FA_ERR_INVALID_ARG;
-  p.status = status_ptr();
+  p.status = status_word();
   if (p.status == nullptr) return FA_ERR_CUDA;
-  cudaError_t e = launch_fwd_mma(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd_tc(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -249,7 +249,7 @@ int fa_backward_dkdv(const void* q, const void* k, const void* v, const float* l
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
-  p.status = status_ptr();
+  p.status = status_word();
   if (p.status == nullptr) return FA_ERR_CUDA;
   const long long rows = (long long)B * H * N;
   cudaError_t e = launch_bwd_mma(p, q, k, v, dout, lse, ws_dvec(workspace),

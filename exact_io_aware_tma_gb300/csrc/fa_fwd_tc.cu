@@ -1,0 +1,421 @@
+// Tensor-core (tcgen05 + TMA) tiled attention forward for sm_103a.
+//
+// One CTA owns two 128-row query tiles of one (b, h) (tiles 2p and 2p+1) and
+// streams the union of their live 128-key tiles (block mask, causal rule,
+// key limit; dead tiles are never loaded) through a ring of shared-memory
+// slots filled by TMA.  The online-softmax recurrence of page
+// "FlashAttention" (aiwiki), section "Tiling and online normalization", is
+// evaluated per query row in log2 units with a lazily moved reference:
+//     m' = max over the tile of scale*log2(e)*q.k_j
+//     if m' > m + 8:  alpha = 2^(m - m'),  m = m'          (else alpha = 1)
+//     p_j = 2^(scale*log2(e)*q.k_j - m),  l = alpha*l + sum_j p_j,
+//     u = alpha*u + sum_j p_j v_j,        O = u / l,  LSE = ln2*(m + log2 l)
+// Keeping m below the running max by at most 8 bounds p_j by 2^8 and leaves
+// u / l unchanged (the reference cancels), so the result is exact up to
+// rounding; it saves most rescalings of the accumulator.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into the slot ring.
+//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM, then
+//               O_i += P_i V_j with P_i read from TMEM; owns TMEM.
+//   warps 4-7   softmax for query tile 0 (TMEM lanes 0-127, one row per thread)
+//   warps 8-11  softmax for query tile 1
+// The softmax warps read S from TMEM, write P (bf16) back over it, rescale
+// O in TMEM when the reference moves, and finally normalise O, store it
+// through shared memory with a TMA store, and write LSE.
+//
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+// MMA order per key tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1); tcgen05 ops of
+// one thread execute in issue order, so S_i(j+1) overwrites P_i(j) only after
+// PV_i(j) has read it, and the commit that signals S_i(j+1) also covers
+// PV_i(j) (the softmax warps may then touch O_i).
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+#include "fa_sm100.cuh"
+#include "fa_tma_host.h"
+
+namespace fa {
+using namespace sm100;
+
+template <int D>
+struct FwdTc {
+  static constexpr int THREADS = 384;
+  static constexpr int NSLOT = D == 64 ? 8 : 4;  // K/V ring slots
+  static constexpr int HALF = 128 * 128;         // one 128-row x 64-col bf16 box
+  static constexpr int TILE = 128 * D * 2;       // one 128-row tile
+  static constexpr int OFF_Q = 0;                // Q0, Q1 (reused for O staging)
+  static constexpr int OFF_KV = 2 * TILE;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+  // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_ready[2],
+  // o_done[2], drain
+  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_S = 1 + 2 * NSLOT,
+                       B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+// Next key tile after kt that is live for query tile q0 or q1 (q1 < 0: absent).
+__device__ __forceinline__ int next_union_tile(const Problem& p, int q0, int q1, int klim,
+                                               int kt) {
+  for (++kt; kt < p.T; ++kt)
+    if (tile_live(p, q0, kt, klim) || (q1 >= 0 && tile_live(p, q1, kt, klim))) return kt;
+  return p.T;
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  Problem p, float* __restrict__ lse) {
+  using C = FwdTc<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t bar0 = s0 + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  const Abort ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int npairs = (p.T + 1) / 2;
+  const int pair = npairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
+  const long long bh = blockIdx.x;
+  const int b = (int)(bh / p.H);
+  const int qt0 = 2 * pair;
+  const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
+  const int klim = key_limit(p, b);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i)
+      mbar_init(bar(i), (i == C::B_P || i == C::B_P + 1) ? 4 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(C::B_Q), (qt1 >= 0 ? 2 : 1) * C::TILE);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(s0 + C::OFF_Q + h * C::HALF, &tm_q, bar(C::B_Q), h * 64, qt0 * 128, (int)bh);
+        if (qt1 >= 0)
+          tma_load_3d(s0 + C::OFF_Q + C::TILE + h * C::HALF, &tm_q, bar(C::B_Q), h * 64,
+                      qt1 * 128, (int)bh);
+      }
+      int slot = 0, round = 0;
+      // per-slot count of loads issued, for the final drain
+      bool ok = true;
+      for (int kt = next_union_tile(p, qt0, qt1, klim, -1); kt < p.T && ok;
+           kt = next_union_tile(p, qt0, qt1, klim, kt)) {
+        for (int which = 0; which < 2; ++which) {
+          if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = s0 + C::OFF_KV + slot * C::TILE;
+          mbar_expect_tx(bar(C::B_FULL + slot), C::TILE);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(dst + h * C::HALF, which == 0 ? &tm_k : &tm_v, bar(C::B_FULL + slot),
+                        h * 64, kt * 128, (int)bh);
+          if (++slot == C::NSLOT) {
+            slot = 0;
+            ++round;
+          }
+        }
+      }
+      // Drain: every load issued must have landed before shared memory is
+      // released (matters only after an abort; otherwise these phases have
+      // completed already).  Slot s was last filled in round
+      // round - (s >= slot ? 1 : 0).
+      for (int s = 0; s < C::NSLOT; ++s) {
+        const int last = round - (s >= slot ? 1 : 0);
+        if (last >= 0) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(bar(C::B_FULL + s), last & 1) &&
+                 globaltimer() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+      {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar(C::B_Q), 0) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
+      const uint32_t q_s[2] = {s0 + C::OFF_Q, s0 + C::OFF_Q + C::TILE};
+      const uint32_t col_s[2] = {C::COL_S0, C::COL_S1};
+      const uint32_t col_o[2] = {C::COL_O0, C::COL_O1};
+      auto issue_qk = [&](int i, uint32_t kslot) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32;
+          mma_ss(tmem + col_s[i], sdesc_sw128(q_s[i] + off, 16, 1024),
+                 sdesc_sw128(kslot + off, 16, 1024), id_qk, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int i, uint32_t vslot, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + col_o[i], tmem + col_s[i] + kk * 8,
+                 sdesc_sw128(vslot + kk * 2048, C::HALF, 1024), id_pv, acc || kk > 0);
+      };
+      int slot = 0, round = 0;
+      auto take = [&](uint32_t& addr, int& bslot, int& par) {
+        addr = s0 + C::OFF_KV + slot * C::TILE;
+        bslot = slot;
+        par = round & 1;
+        if (++slot == C::NSLOT) {
+          slot = 0;
+          ++round;
+        }
+      };
+      bool ok = mbar_wait(bar(C::B_Q), 0, ab);
+      tc_fence_after();
+      int cur = next_union_tile(p, qt0, qt1, klim, -1);
+      int npv[2] = {0, 0};
+      uint32_t kaddr;
+      int kslot, kpar;
+      if (ok && cur < p.T) {
+        take(kaddr, kslot, kpar);
+        ok = mbar_wait(bar(C::B_FULL + kslot), kpar, ab);
+        tc_fence_after();
+        if (ok) {
+          if (tile_live(p, qt0, cur, klim)) {
+            issue_qk(0, kaddr);
+            mma_commit(bar(C::B_S + 0));
+          }
+          if (qt1 >= 0 && tile_live(p, qt1, cur, klim)) {
+            issue_qk(1, kaddr);
+            mma_commit(bar(C::B_S + 1));
+          }
+          mma_commit(bar(C::B_EMPTY + kslot));
+        }
+      }
+      while (ok && cur < p.T) {
+        const bool l0 = tile_live(p, qt0, cur, klim);
+        const bool l1 = qt1 >= 0 && tile_live(p, qt1, cur, klim);
+        uint32_t vaddr;
+        int vslot, vpar;
+        take(vaddr, vslot, vpar);
+        const int nxt = next_union_tile(p, qt0, qt1, klim, cur);
+        const bool has_next = nxt < p.T;
+        const bool n0 = has_next && tile_live(p, qt0, nxt, klim);
+        const bool n1 = has_next && qt1 >= 0 && tile_live(p, qt1, nxt, klim);
+        uint32_t naddr = 0;
+        int nslot = 0, npar = 0;
+        if (has_next) take(naddr, nslot, npar);
+        if (!(ok = mbar_wait(bar(C::B_FULL + vslot), vpar, ab))) break;
+        tc_fence_after();
+        if (l0) {
+          if (!(ok = mbar_wait(bar(C::B_P + 0), npv[0] & 1, ab))) break;
+          tc_fence_after();
+          issue_pv(0, vaddr, npv[0] > 0);
+          ++npv[0];
+        }
+        if (has_next) {
+          if (!(ok = mbar_wait(bar(C::B_FULL + nslot), npar, ab))) break;
+          tc_fence_after();
+          if (n0) {
+            issue_qk(0, naddr);
+            mma_commit(bar(C::B_S + 0));
+          }
+        }
+        if (l1) {
+          if (!(ok = mbar_wait(bar(C::B_P + 1), npv[1] & 1, ab))) break;
+          tc_fence_after();
+          issue_pv(1, vaddr, npv[1] > 0);
+          ++npv[1];
+        }
+        mma_commit(bar(C::B_EMPTY + vslot));
+        if (has_next) {
+          if (n1) {
+            issue_qk(1, naddr);
+            mma_commit(bar(C::B_S + 1));
+          }
+          mma_commit(bar(C::B_EMPTY + nslot));
+        }
+        cur = nxt;
+      }
+      mma_commit(bar(C::B_O + 0));
+      mma_commit(bar(C::B_O + 1));
+      // Drain all issued tensor-core work before TMEM can be released.
+      mma_commit(bar(C::B_DRAIN));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int i = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int qt = i == 0 ? qt0 : qt1;
+    if (qt >= 0) {
+      const int r = ((warp & 3) << 5) + lane;  // row within the tile = TMEM lane
+      const int row = qt * 128 + r;
+      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      const uint32_t col_s = i == 0 ? C::COL_S0 : C::COL_S1;
+      const uint32_t col_o = i == 0 ? C::COL_O0 : C::COL_O1;
+      const float cl2 = p.scale_log2;
+      float m_ref = -INFINITY, l = 0.f;
+      int n = 0;
+      bool ok = true;
+      for (int kt = next_union_tile(p, qt0, qt1, klim, -1); kt < p.T;
+           kt = next_union_tile(p, qt0, qt1, klim, kt)) {
+        if (!tile_live(p, qt, kt, klim)) continue;
+        if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(lane_base + col_s + 32 * c, raw);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]);
+        }
+        const bool diag = p.causal && kt == qt;
+        if (diag || (kt + 1) * 128 > klim) {
+          int lim = klim - kt * 128;
+          if (diag && r + 1 < lim) lim = r + 1;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        float mx = -INFINITY;
+        if (cl2 >= 0.f) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        } else {
+          float mn = INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) mn = fminf(mn, s[c] == -INFINITY ? INFINITY : s[c]);
+          mx = mn == INFINITY ? -INFINITY : mn;
+        }
+        const float m_tile = mx == -INFINITY ? -INFINITY : mx * cl2;
+        float alpha = 1.f;
+        if (m_tile > m_ref + 8.f) {
+          alpha = fast_exp2(m_ref - m_tile);  // 0 when m_ref = -inf
+          m_ref = m_tile;
+        }
+        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = fast_exp2(fmaf(s[32 * c + 2 * j], cl2, -ref));
+            const float p1 = fast_exp2(fmaf(s[32 * c + 2 * j + 1], cl2, -ref));
+            sum += p0 + p1;
+            pk[j] = pack_bf16(p0, p1);
+          }
+          tmem_st16(lane_base + col_s + 16 * c, pk);
+        }
+        l = l * alpha + sum;
+        if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + col_o + 32 * c, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(lane_base + col_o + 32 * c, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_P + i));
+        ++n;
+      }
+      // ---- epilogue: O = u / l -> bf16 -> shared (swizzled) -> TMA store
+      if (ok) ok = mbar_wait(bar(C::B_O + i), 0, ab);
+      tc_fence_after();
+      uint8_t* stage = smem + C::OFF_Q + i * C::TILE;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + col_o + 32 * c, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          // 32 columns = four 16-byte chunks, chunk index cc = 4c + q
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int cc = 4 * c + q;
+            uint8_t* dst = stage + (cc >> 3) * C::HALF + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        if (row < p.N)
+          lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      }
+      fence_proxy_async_smem();
+      named_barrier(1 + i, 128);
+      if (ok && r == 0) {
+        for (int h = 0; h < D / 64; ++h)
+          tma_store_3d(&tm_o, smem_u32(stage) + h * C::HALF, h * 64, qt * 128, (int)bh);
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
+                                   void* o, float* lse, cudaStream_t st) {
+  using C = FwdTc<D>;
+  const long long bh = (long long)p.B * p.H;
+  CUtensorMap tq, tk, tv, to;
+  if (!make_bf16_map_3d(&tq, q, D, p.N, bh, 128) || !make_bf16_map_3d(&tk, k, D, p.N, bh, 128) ||
+      !make_bf16_map_3d(&tv, v, D, p.N, bh, 128) || !make_bf16_map_3d(&to, o, D, p.N, bh, 128))
+    return cudaErrorInvalidValue;
+  auto kern = fwd_tc_kernel<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)bh, (unsigned)((p.T + 1) / 2));
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, to, p, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                          float* lse, cudaStream_t st) {
+  return p.d == 64 ? launch_fwd_tc_t<64>(p, q, k, v, o, lse, st)
+                   : launch_fwd_tc_t<128>(p, q, k, v, o, lse, st);
+}
+
+}  // namespace fa

@@ -7,8 +7,10 @@
 
 namespace fa {
 
-cudaError_t launch_fwd_mma(const Problem& p, const void* q, const void* k, const void* v,
-                           void* o, float* lse, cudaStream_t st);
+cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          void* o, float* lse, cudaStream_t st);
+
+int* status_word();
 
 cudaError_t launch_bwd_mma(const Problem& p, const void* q, const void* k, const void* v,
                            const void* dout, const float* lse, const float* dvec,

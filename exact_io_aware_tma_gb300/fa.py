@@ -29,6 +29,7 @@ SIGNATURES = {
     "fa_backward_dq_convert": ([_vp] + [_i] * 4 + [_f, _vp, _sz, _vp], _i),
     "fa_tile_schedule": ([_i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
     "fa_last_device_status": ([_vp], _i),
+    "fa_selftest_mma": ([_i, _vp, _vp, _vp, _i, _vp], _i),
 }
 
 
@@ -153,3 +154,15 @@ def tile_schedule(N, causal=False, block_mask=None, kv_len=None, b=0, device="cu
 
 def last_device_status(stream=None):
     return int(load().fa_last_device_status(_stream(stream)))
+
+
+def selftest_mma(mode, a, b, n=128, stream=None):
+    """Single-tile tensor-core self-test (include/fa_selftest.h); returns c."""
+    lib = load()
+    rows = 128
+    cols = 128 if mode == 0 else n
+    c = torch.full((rows, cols), float("nan"), device=a.device, dtype=torch.float32)
+    st = lib.fa_selftest_mma(int(mode), _ptr(a), _ptr(b), _ptr(c), int(n), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_selftest_mma")
+    return c

@@ -1,0 +1,41 @@
+/*
+ * fa_selftest.h -- tensor-core self-test of the attention library.
+ *
+ * Not part of the attention method: a check of the sm_103a building blocks
+ * the attention kernels are assembled from, on one 128-row tile, so that a
+ * wrong operand layout is caught in isolation.  All pointers are device
+ * pointers; the call is asynchronous on `stream`.
+ *
+ *   a : bf16 [128][128] row-major.
+ *   b : mode 0: bf16 [128][128] row-major (one row per output column);
+ *       modes 1-3: bf16 [128][n] row-major.
+ *   c : fp32 [128][n] row-major output (n = 128 in mode 0).
+ *   mode 0: c = a * b^T  (both operands K-major in shared memory via TMA;
+ *           the S = Q K^T path).
+ *   mode 1: c = a * b    (a K-major via TMA, b MN-major via TMA; the
+ *           O += P V path with P in shared memory).
+ *   mode 2: c = a * b    (a written to tensor memory by tcgen05.st, b
+ *           MN-major via TMA; the O += P V path with P in tensor memory).
+ *   mode 3: c = a * b    (a written to shared memory by threads in the
+ *           128-byte-swizzled layout, b MN-major via TMA).
+ *   n    : 64 or 128 (modes 1-3).
+ * Returns 0 on success, 1 on a bad argument, 3 on a CUDA error.  A bounded
+ * wait that gives up is reported by fa_last_device_status().
+ */
+#ifndef FA_GB300_SELFTEST_H
+#define FA_GB300_SELFTEST_H
+
+#include "fa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+FA_API int fa_selftest_mma(int mode, const void* a, const void* b, float* c, int n,
+                           void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_SELFTEST_H */

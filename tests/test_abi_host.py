@@ -9,7 +9,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "fa.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,8 +23,10 @@ def lib():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
-    return re.findall(r"FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", text)
+    out = []
+    for h in HEADERS:
+        out += re.findall(r"FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", open(h).read())
+    return out
 
 
 def test_header_declares_the_entry_points():

@@ -1,0 +1,25 @@
+"""Unit checks of the tensor-core building blocks on one 128-row tile
+(include/fa_selftest.h) against a float64 matmul of the same bf16 values.
+Each mode is one operand path of the attention kernels."""
+
+import pytest
+import torch
+
+from exact_io_aware_tma_gb300 import fa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("mode,n", [(0, 128), (1, 64), (1, 128), (2, 64), (2, 128),
+                                    (3, 64), (3, 128)])
+def test_single_tile_mma(mode, n):
+    g = torch.Generator().manual_seed(100 + 10 * mode + n)
+    a = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    b = torch.randn(128, 128 if mode == 0 else n, generator=g).to(torch.bfloat16).cuda()
+    c = fa.selftest_mma(mode, a, b, n)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    ref = a.double() @ (b.double().T if mode == 0 else b.double())
+    err = (c.double() - ref).abs().max().item()
+    # fp32 accumulation of 128 exact bf16 products
+    assert err <= 1e-5 * ref.abs().max().item() * 16, (mode, n, err)
