@@ -249,9 +249,9 @@ def run_gpu(args, cfg, name):
         st = [lib.fa_forward(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, int(causal),
                              bmp, kvp, sp)]
         ev[i][1].record(stream)
-        st.append(lib.fa_backward_preprocess(P(o), P(do), B, H, N, d, P(ws), wsb, sp))
+        st.append(lib.fa_backward_preprocess(P(o), P(do), P(lse), B, H, N, d, P(ws), wsb, sp))
         ev[i][2].record(stream)
-        st.append(lib.fa_backward_dkdv(P(q), P(k), P(v), P(lse), P(do), P(dk), P(dv), B, H,
+        st.append(lib.fa_backward_dkdv(P(q), P(k), P(v), P(do), P(dk), P(dv), B, H,
                                        N, d, scale, int(causal), bmp, kvp, P(ws), wsb, sp))
         ev[i][3].record(stream)
         st.append(lib.fa_backward_dq_convert(P(dq), B, H, N, d, scale, P(ws), wsb, sp))

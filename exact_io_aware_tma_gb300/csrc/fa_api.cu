@@ -15,24 +15,33 @@ namespace fa {
 __device__ int g_fa_status = 0;
 
 // ---------------------------------------------------------------------------
-// Backward preprocess: D_i = sum_c dO_ic * O_ic (fp32) and dQacc = 0.
-// One thread per 16-byte chunk (8 bf16) of a row; the CH chunks of a row are
-// adjacent lanes of one warp and are reduced by shuffles.
+// Backward preprocess.  Per query row (padded per head to a multiple of 128
+// rows): D_i = sum_c dO_ic * O_ic and L_i = LSE_i * log2(e), written as +inf
+// for rows without an allowed key and for padding rows (so every
+// probability the backward rebuilds for them is 2^-inf = 0), D = 0 there;
+// also clears the fp32 dQ accumulator.  One thread per 16-byte chunk (8 bf16)
+// of a row; the CH chunks of a row are adjacent lanes and reduce by shuffles.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
-                          const __nv_bfloat16* __restrict__ dout, float* __restrict__ dvec,
-                          float* __restrict__ dq_acc, long long rows) {
+                          const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                          float* __restrict__ lse2, float* __restrict__ dvec,
+                          float* __restrict__ dq_acc, long long heads, int N, int npad) {
   constexpr int CH = D / 8;
-  const long long n = rows * CH;
+  const long long n = heads * npad * CH;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n;
        i += (long long)gridDim.x * blockDim.x) {
     float acc = 0.f;
-    const bool ok = i < n;
-    if (ok) {
-      uint4 a = *reinterpret_cast<const uint4*>(o + i * 8);
-      uint4 b = *reinterpret_cast<const uint4*>(dout + i * 8);
+    const bool in = i < n;
+    const long long prow = i / CH;  // padded row index
+    const long long bh = prow / npad;
+    const int row = (int)(prow % npad);
+    const bool live = in && row < N;
+    if (live) {
+      const long long e = ((bh * N + row) * CH + (i % CH)) * 8;
+      uint4 a = *reinterpret_cast<const uint4*>(o + e);
+      uint4 b = *reinterpret_cast<const uint4*>(dout + e);
       const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
       const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -43,12 +52,16 @@ __global__ void __launch_bounds__(256)
         acc = fmaf(x.y, y.y, acc);
       }
       float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      reinterpret_cast<float4*>(dq_acc + i * 8)[0] = z;
-      reinterpret_cast<float4*>(dq_acc + i * 8)[1] = z;
+      reinterpret_cast<float4*>(dq_acc + e)[0] = z;
+      reinterpret_cast<float4*>(dq_acc + e)[1] = z;
     }
 #pragma unroll
     for (int off = CH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (ok && (i % CH) == 0) dvec[i / CH] = acc;
+    if (in && (i % CH) == 0) {
+      dvec[prow] = live ? acc : 0.f;
+      const float l = live ? lse[bh * N + row] : -INFINITY;
+      lse2[prow] = l == -INFINITY ? INFINITY : l * kLog2e;
+    }
   }
 }
 
@@ -153,6 +166,7 @@ static int check_sizes(int B, int H, int N, int d, float scale, int causal,
 }
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+static int padded_rows(int N) { return (N + kTile - 1) / kTile * kTile; }
 
 }  // namespace fa
 
@@ -190,8 +204,8 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   Problem p;
   if (check_sizes(B, H, N, d, 1.0f, 0, nullptr, nullptr, &p) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return round_up(rows * sizeof(float), 256) + round_up(rows * d * sizeof(float), 256);
+  const size_t vec = round_up((size_t)B * H * padded_rows(N) * sizeof(float), 256);
+  return 2 * vec + round_up((size_t)B * H * N * d * sizeof(float), 256);
 }
 
 static int check_workspace(int B, int H, int N, int d, const void* ws, size_t wsb) {
@@ -200,10 +214,17 @@ static int check_workspace(int B, int H, int N, int d, const void* ws, size_t ws
   return FA_OK;
 }
 
-static float* ws_dvec(void* ws) { return static_cast<float*>(ws); }
-static float* ws_dq_acc(void* ws, long long rows) {
-  return reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                  round_up((size_t)rows * sizeof(float), 256));
+// Workspace: L = LSE*log2(e) [B*H][Np], D [B*H][Np] (Np = N rounded up to
+// 128), then the fp32 dQ accumulator [B*H][N][d].
+static size_t ws_vec_bytes(long long heads, int N) {
+  return round_up((size_t)heads * padded_rows(N) * sizeof(float), 256);
+}
+static float* ws_lse2(void* ws) { return static_cast<float*>(ws); }
+static float* ws_dvec(void* ws, long long heads, int N) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + ws_vec_bytes(heads, N));
+}
+static float* ws_dq_acc(void* ws, long long heads, int N) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ws_vec_bytes(heads, N));
 }
 
 // Elementwise kernels: enough CTAs for every chunk, capped at a few waves.
@@ -213,48 +234,52 @@ static unsigned elementwise_blocks(long long chunks) {
   return (unsigned)(nblk < 1 ? 1 : nblk);
 }
 
-int fa_backward_preprocess(const void* o, const void* dout, int B, int H, int N, int d,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+int fa_backward_preprocess(const void* o, const void* dout, const float* lse, int B, int H,
+                           int N, int d, void* workspace, size_t workspace_bytes, void* stream) {
   Problem p;
   int st = check_sizes(B, H, N, d, 1.0f, 0, nullptr, nullptr, &p);
   if (st != FA_OK) return st;
-  if (!o || !dout || !aligned(o, 16) || !aligned(dout, 16)) return FA_ERR_INVALID_ARG;
+  if (!o || !dout || !lse || !aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const long long rows = (long long)B * H * N;
-  const unsigned nblk = elementwise_blocks(rows * (d / 8));
+  const long long heads = (long long)B * H;
+  const int npad = padded_rows(N);
+  const unsigned nblk = elementwise_blocks(heads * npad * (d / 8));
   auto ob = static_cast<const __nv_bfloat16*>(o);
   auto db = static_cast<const __nv_bfloat16*>(dout);
   if (d == 64)
-    bwd_preprocess_kernel<64><<<nblk, 256, 0, s>>>(ob, db, ws_dvec(workspace),
-                                                   ws_dq_acc(workspace, rows), rows);
+    bwd_preprocess_kernel<64><<<nblk, 256, 0, s>>>(ob, db, lse, ws_lse2(workspace),
+                                                   ws_dvec(workspace, heads, N),
+                                                   ws_dq_acc(workspace, heads, N), heads, N, npad);
   else
-    bwd_preprocess_kernel<128><<<nblk, 256, 0, s>>>(ob, db, ws_dvec(workspace),
-                                                    ws_dq_acc(workspace, rows), rows);
+    bwd_preprocess_kernel<128><<<nblk, 256, 0, s>>>(ob, db, lse, ws_lse2(workspace),
+                                                    ws_dvec(workspace, heads, N),
+                                                    ws_dq_acc(workspace, heads, N), heads, N, npad);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_backward_dkdv(const void* q, const void* k, const void* v, const float* lse,
-                     const void* dout, void* dk, void* dv, int B, int H, int N, int d,
+int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                     void* dv, int B, int H, int N, int d,
                      float scale, int causal, const uint8_t* block_mask,
                      const int32_t* kv_len, void* workspace, size_t workspace_bytes,
                      void* stream) {
   Problem p;
   int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
   if (st != FA_OK) return st;
-  if (!q || !k || !v || !lse || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) ||
-      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(kv_len, 4))
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(kv_len, 4))
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   p.status = status_word();
   if (p.status == nullptr) return FA_ERR_CUDA;
-  const long long rows = (long long)B * H * N;
-  cudaError_t e = launch_bwd_mma(p, q, k, v, dout, lse, ws_dvec(workspace),
-                                 ws_dq_acc(workspace, rows), dk, dv,
-                                 static_cast<cudaStream_t>(stream));
+  const long long heads = (long long)B * H;
+  cudaError_t e = launch_bwd_tc(p, q, k, v, dout, ws_lse2(workspace),
+                                ws_dvec(workspace, heads, N), ws_dq_acc(workspace, heads, N),
+                                dk, dv, padded_rows(N), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -266,10 +291,10 @@ int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
   if (!dq || !aligned(dq, 16)) return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
-  const long long rows = (long long)B * H * N;
-  const long long chunks = rows * (d / 8);
+  const long long heads = (long long)B * H;
+  const long long chunks = heads * N * (d / 8);
   dq_convert_kernel<<<elementwise_blocks(chunks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      ws_dq_acc(const_cast<void*>(workspace), rows), static_cast<__nv_bfloat16*>(dq), scale,
+      ws_dq_acc(const_cast<void*>(workspace), heads, N), static_cast<__nv_bfloat16*>(dq), scale,
       chunks);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -291,10 +316,10 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o,
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
-  st = fa_backward_preprocess(o, dout, B, H, N, d, workspace, workspace_bytes, stream);
+  st = fa_backward_preprocess(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream);
   if (st != FA_OK) return st;
-  st = fa_backward_dkdv(q, k, v, lse, dout, dk, dv, B, H, N, d, scale, causal, block_mask,
-                        kv_len, workspace, workspace_bytes, stream);
+  st = fa_backward_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, causal, block_mask, kv_len,
+                        workspace, workspace_bytes, stream);
   if (st != FA_OK) return st;
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }

@@ -1,0 +1,438 @@
+// Tensor-core (tcgen05 + TMA) attention backward with recomputation, sm_103a.
+//
+// One CTA owns one 128-key tile of one (b, h).  K and V are loaded once; the
+// CTA walks the live query tiles of its key tile in 64-row steps.  Per step
+// i (queries q0 .. q0+63) it rebuilds the probabilities from the stored row
+// statistic instead of reading a stored P (page "FlashAttention IO-aware
+// explained", section "Recomputation and IO complexity"; Theorem 5's proof
+// on page "FlashAttention: Fast and Memory-Efficient Exact Attention with
+// IO-Awareness", "C Proofs": K, V read once, passes over Q, O, dO, dQ):
+//     S^T  = K Q^T              (TMEM, 128 x 64)
+//     dP^T = V dO^T             (TMEM, 128 x 64)
+//     P^T  = 2^(scale*log2e*S^T - LSE*log2e)     (masked; bf16 back to TMEM)
+//     dS^T = P^T * (dP^T - D)                    (bf16 to shared memory)
+//     dV  += P^T dO             (A = P^T from TMEM)
+//     dK  += dS^T Q             (scaled by `scale` in the epilogue)
+//     dQ^T = K^T dS^T           (TMEM, d x 64; reduce-added into the fp32 dQ
+//                                accumulator by a TMA reduce; the conversion
+//                                kernel applies `scale`)
+// with D = rowsum(dO * O) and LSE*log2e precomputed per query row.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: K, V once; per step Q, dO (64 rows) and the
+//               64 LSE / D values into a ring of stages.
+//   warp 1      MMA issuer (one thread); owns TMEM.
+//   warps 4-7   element-wise: P^T, dS^T (one key row per thread); at the
+//               end dK, dV from TMEM to bf16 and a TMA store.
+//   warps 8-11  dQ: dQ^T from TMEM (one head-dim row per thread) to shared
+//               memory, then TMA reduce-adds of two 32 x d fp32 tiles.
+//
+// TMEM columns: dV [0,d), dK [d,2d), S[b] = 2d + 64b, dP[b] = 2d + 128 + 64b
+// for the two step buffers b; dQ^T of step i is written over dP[i % 2] once
+// the element-wise warps have consumed dP^T(i), and dP^T(i+2) waits until
+// the dQ warps have read dQ^T(i) out.  For d = 64 the dQ^T product is issued
+// with M = 128 (the second 64 rows read the V tile and are discarded).
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "fa_kernels.h"
+#include "fa_sm100.cuh"
+#include "fa_tma_host.h"
+
+namespace fa {
+using namespace sm100;
+
+template <int D>
+struct BwdTc {
+  static constexpr int THREADS = 384;
+  static constexpr int BQ = 64;                 // query rows per step
+  static constexpr int NS = D == 128 ? 3 : 4;   // step stages
+  static constexpr int HALF_K = 128 * 128;      // [128 rows][64 cols] bf16 box
+  static constexpr int HALF_Q = 64 * 128;       // [64 rows][64 cols] bf16 box
+  static constexpr int KT = 128 * D * 2;        // K or V tile
+  static constexpr int QB = BQ * D * 2;         // Q or dO block
+  static constexpr int STAGE = 2 * QB;          // Q, dO of one step
+  static constexpr int OFF_K = 0, OFF_V = KT, OFF_ST = 2 * KT;
+  static constexpr int OFF_VEC = OFF_ST + NS * STAGE;  // [NS][LSE*log2e (64), D (64)]
+  static constexpr int OFF_DS = (OFF_VEC + NS * 512 + 1023) / 1024 * 1024;
+  static constexpr int DS = 128 * BQ * 2;             // dS^T [128 keys][64 q] bf16, x2
+  static constexpr int OFF_DQ = OFF_DS + 2 * DS;      // fp32 [32 q][D] staging
+  static constexpr int DQ_ROWS = 32;                  // dQ reduce-add box height
+  static constexpr int DQB = DQ_ROWS * D * 4;
+  static constexpr int OFF_BAR = OFF_DQ + DQB;
+  static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_S = 1 + 2 * NS, B_EW = B_S + 2,
+                       B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_FIN = B_DQE + 2,
+                       B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 32 + 1024;
+  static constexpr int COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(2 * KT <= NS * STAGE, "dK/dV staging must fit in the stage ring");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// Next 64-row query step after (qt, sub) for key tile kt: live query tiles
+// in ascending order, two halves each, skipping halves past N.
+__device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, int& qt,
+                                            int& sub) {
+  if (qt >= 0 && sub == 0 && qt * 128 + 64 < p.N) {
+    sub = 1;
+    return true;
+  }
+  sub = 0;
+  for (++qt; qt < p.T; ++qt)
+    if (tile_live(p, qt, kt, klim)) return true;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                  const __grid_constant__ CUtensorMap tm_dq, Problem p,
+                  const float* __restrict__ lse2, const float* __restrict__ dvec, int npad) {
+  using C = BwdTc<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t bar0 = s0 + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+  const Abort ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long bh = blockIdx.x;
+  const int kt = blockIdx.y;  // small key tiles carry the most causal work: first
+  const int b = (int)(bh / p.H);
+  const int klim = key_limit(p, b);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const bool four = (i == C::B_EW || i == C::B_EW + 1 || i == C::B_DQE || i == C::B_DQE + 1);
+      mbar_init(bar(i), four ? 4 : 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+    prefetch_tensormap(&tm_dq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const size_t vec_base = (size_t)bh * npad;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(C::B_KV), 2 * C::KT);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(s0 + C::OFF_K + h * C::HALF_K, &tm_k, bar(C::B_KV), h * 64, kt * 128, (int)bh);
+        tma_load_3d(s0 + C::OFF_V + h * C::HALF_K, &tm_v, bar(C::B_KV), h * 64, kt * 128, (int)bh);
+      }
+      int qt = -1, sub = 0, slot = 0, round = 0;
+      while (next_q_step(p, kt, klim, qt, sub)) {
+        const int q0 = qt * 128 + sub * 64;
+        if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) break;
+        const uint32_t st = s0 + C::OFF_ST + slot * C::STAGE;
+        const uint32_t fb = bar(C::B_FULL + slot);
+        const uint32_t vb = s0 + C::OFF_VEC + slot * 512;
+        mbar_expect_tx(fb, 2 * C::QB + 512);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(st + h * C::HALF_Q, &tm_q, fb, h * 64, q0, (int)bh);
+          tma_load_3d(st + C::QB + h * C::HALF_Q, &tm_do, fb, h * 64, q0, (int)bh);
+        }
+        bulk_load(vb, lse2 + vec_base + q0, 256, fb);
+        bulk_load(vb + 256, dvec + vec_base + q0, 256, fb);
+        if (++slot == C::NS) {
+          slot = 0;
+          ++round;
+        }
+      }
+      // Drain every load issued before shared memory is released.
+      for (int s = 0; s < C::NS; ++s) {
+        const int last = round - (s >= slot ? 1 : 0);
+        if (last >= 0) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(bar(C::B_FULL + s), last & 1) &&
+                 globaltimer() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar(C::B_KV), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, C::BQ, false, false);
+      constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
+      constexpr uint32_t id_q = idesc_bf16(128, C::BQ, true, true);
+      const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V;
+      auto stage_addr = [&](int i) { return s0 + C::OFF_ST + (i % C::NS) * C::STAGE; };
+      bool ok = mbar_wait(bar(C::B_KV), 0, ab);
+      tc_fence_after();
+      // S^T and dP^T of step j into buffer j % 2.
+      auto issue_sdp = [&](int j) -> bool {
+        const int bf = j & 1;
+        const uint32_t st = stage_addr(j);
+        if (!mbar_wait(bar(C::B_FULL + j % C::NS), (j / C::NS) & 1, ab)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * C::HALF_K + (kk & 3) * 32;
+          const uint32_t qa = (kk >> 2) * C::HALF_Q + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_S + 64 * bf, sdesc_sw128(sK + ka, 16, 1024),
+                 sdesc_sw128(st + qa, 16, 1024), id_s, kk > 0);
+        }
+        if (j >= 2) {
+          if (!mbar_wait(bar(C::B_DQE + bf), ((j - 2) >> 1) & 1, ab)) return false;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * C::HALF_K + (kk & 3) * 32;
+          const uint32_t qa = (kk >> 2) * C::HALF_Q + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_DP + 64 * bf, sdesc_sw128(sV + ka, 16, 1024),
+                 sdesc_sw128(st + C::QB + qa, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(bar(C::B_S + bf));
+        return true;
+      };
+      int qa_t = -1, qa_s = 0;  // iterator for the S/dP lookahead
+      int issued = 0;
+      for (int w = 0; w < 2 && ok && next_q_step(p, kt, klim, qa_t, qa_s); ++w) {
+        ok = issue_sdp(issued);
+        ++issued;
+      }
+      int qi_t = -1, qi_s = 0;
+      for (int i = 0; ok && next_q_step(p, kt, klim, qi_t, qi_s); ++i) {
+        const int bf = i & 1;
+        const uint32_t st = stage_addr(i);
+        if (!(ok = mbar_wait(bar(C::B_EW + bf), (i >> 1) & 1, ab))) break;
+        tc_fence_after();
+        // dV += P^T dO   (P^T: bf16 in TMEM over S[bf])
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 64 * bf + kk * 8,
+                 sdesc_sw128(st + C::QB + kk * 2048, C::HALF_Q, 1024), id_kv, (i > 0) || (kk > 0));
+        // dK += dS^T Q
+        const uint32_t ds = s0 + C::OFF_DS + bf * C::DS;
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ss(tmem + C::COL_DK, sdesc_sw128(ds + kk * 32, 16, 1024),
+                 sdesc_sw128(st + kk * 2048, C::HALF_Q, 1024), id_kv, (i > 0) || (kk > 0));
+        mma_commit(bar(C::B_EMPTY + i % C::NS));
+        // dQ^T = K^T dS^T over dP[bf]
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::COL_DP + 64 * bf, sdesc_sw128(sK + kk * 2048, C::HALF_K, 1024),
+                 sdesc_sw128(ds + kk * 2048, 16, 1024), id_q, kk > 0);
+        mma_commit(bar(C::B_DQF + bf));
+        if (next_q_step(p, kt, klim, qa_t, qa_s)) {
+          if (!(ok = issue_sdp(issued))) break;
+          ++issued;
+        }
+      }
+      mma_commit(bar(C::B_FIN));
+      mma_commit(bar(C::B_DRAIN));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ element-wise
+    const int r = ((warp & 3) << 5) + lane;  // key row within the tile
+    const int j = kt * 128 + r;              // key index
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const float cl2 = p.scale_log2;
+    int qt = -1, sub = 0, i = 0;
+    bool ok = true;
+    for (; next_q_step(p, kt, klim, qt, sub); ++i) {
+      const int bf = i & 1;
+      const int q0 = qt * 128 + sub * 64;
+      const uint8_t* vb = smem + C::OFF_VEC + (i % C::NS) * 512;
+      const float* l2 = reinterpret_cast<const float*>(vb);
+      const float* dv = reinterpret_cast<const float*>(vb + 256);
+      if (!(ok = mbar_wait(bar(C::B_S + bf), (i >> 1) & 1, ab))) break;
+      tc_fence_after();
+      uint32_t sr[64], pr[64];
+      tmem_ld32(lane_base + C::COL_S + 64 * bf, sr);
+      tmem_ld32(lane_base + C::COL_S + 64 * bf + 32, sr + 32);
+      tmem_ld32(lane_base + C::COL_DP + 64 * bf, pr);
+      tmem_ld32(lane_base + C::COL_DP + 64 * bf + 32, pr + 32);
+      // queries c allowed for this key: c >= lo (causal) and key < klim
+      int lo = 0;
+      if (j >= klim) lo = 64;
+      else if (p.causal && j > q0) lo = j - q0;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 L = reinterpret_cast<const float4*>(l2)[c4];
+        const float4 Dd = reinterpret_cast<const float4*>(dv)[c4];
+        const float lv[4] = {L.x, L.y, L.z, L.w};
+        const float dd[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          float pe = fast_exp2(fmaf(__uint_as_float(sr[c]), cl2, -lv[e]));
+          if (c < lo) pe = 0.f;
+          pv[e] = pe;
+          dsv[e] = pe * (__uint_as_float(pr[c]) - dd[e]);
+        }
+        pk[2 * c4] = pack_bf16(pv[0], pv[1]);
+        pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
+        dk[2 * c4] = pack_bf16(dsv[0], dsv[1]);
+        dk[2 * c4 + 1] = pack_bf16(dsv[2], dsv[3]);
+      }
+      tmem_st32(lane_base + C::COL_S + 64 * bf, pk);
+      // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of
+      // step i-2 (which read this buffer) have completed.
+      if (i >= 2) {
+        if (!(ok = mbar_wait(bar(C::B_DQF + bf), ((i - 2) >> 1) & 1, ab))) break;
+      }
+      uint8_t* dsb = smem + C::OFF_DS + bf * C::DS + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        *reinterpret_cast<uint4*>(dsb + ((c8 ^ (r & 7)) << 4)) =
+            make_uint4(dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_EW + bf));
+    }
+    // ---- epilogue: dK (x scale), dV -> bf16 -> shared (swizzled) -> TMA store
+    if (ok) ok = mbar_wait(bar(C::B_FIN), 0, ab);
+    tc_fence_after();
+    uint8_t* stg = smem + C::OFF_ST;  // dK tile, then dV tile
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t col = t == 0 ? C::COL_DK : C::COL_DV;
+      const float mul = t == 0 ? p.scale : 1.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (i > 0 && ok) {
+          tmem_ld32(lane_base + col + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        uint32_t pw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pw[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = 4 * c + q;
+          uint8_t* dst = stg + t * C::KT + (cc >> 3) * C::HALF_K + r * 128 +
+                         (((cc & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    if (ok && r == 0) {
+      for (int h = 0; h < D / 64; ++h) {
+        tma_store_3d(&tm_dk, smem_u32(stg) + h * C::HALF_K, h * 64, kt * 128, (int)bh);
+        tma_store_3d(&tm_dv, smem_u32(stg) + C::KT + h * C::HALF_K, h * 64, kt * 128, (int)bh);
+      }
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ
+    const int c = ((warp & 3) << 5) + lane;  // head-dim index = TMEM lane
+    const bool valid = c < D;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int t = threadIdx.x - 256;  // 0..127 within the warpgroup
+    float* stg = reinterpret_cast<float*>(smem + C::OFF_DQ);
+    int qt = -1, sub = 0;
+    bool ok = true;
+    for (int i = 0; next_q_step(p, kt, klim, qt, sub); ++i) {
+      const int bf = i & 1;
+      const int q0 = qt * 128 + sub * 64;
+      if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab))) break;
+      tc_fence_after();
+      uint32_t v[64];
+      if (valid) {
+        tmem_ld32(lane_base + C::COL_DP + 64 * bf, v);
+        tmem_ld32(lane_base + C::COL_DP + 64 * bf + 32, v + 32);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_DQE + bf));
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        // the staging tile is free once the previous reduce has read it
+        if (t == 0 && (i > 0 || hh > 0)) tma_store_wait_read();
+        named_barrier(2, 128);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < C::DQ_ROWS; ++q)
+            stg[q * D + c] = __uint_as_float(v[hh * C::DQ_ROWS + q]);
+        }
+        fence_proxy_async_smem();
+        named_barrier(2, 128);
+        if (t == 0) {
+          tma_reduce_add_3d(&tm_dq, smem_u32(stg), 0, q0 + hh * C::DQ_ROWS, (int)bh);
+          tma_store_commit();
+        }
+      }
+    }
+    if (t == 0) tma_store_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
+                                   const void* dout, const float* lse2, const float* dvec,
+                                   float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
+  using C = BwdTc<D>;
+  const long long bh = (long long)p.B * p.H;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+  if (!make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) || !make_bf16_map_3d(&tk, k, D, p.N, bh, 128) ||
+      !make_bf16_map_3d(&tv, v, D, p.N, bh, 128) ||
+      !make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) ||
+      !make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) || !make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128) ||
+      !make_f32_map_3d(&tdq, dq_acc, D, p.N, bh, C::DQ_ROWS))
+    return cudaErrorInvalidValue;
+  auto kern = bwd_tc_kernel<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)bh, (unsigned)p.T);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, lse2, dvec, npad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          const void* dout, const float* lse2, const float* dvec, float* dq_acc,
+                          void* dk, void* dv, int npad, cudaStream_t st) {
+  return p.d == 64 ? launch_bwd_tc_t<64>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
+                   : launch_bwd_tc_t<128>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st);
+}
+
+}  // namespace fa

@@ -12,8 +12,8 @@ cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const 
 
 int* status_word();
 
-cudaError_t launch_bwd_mma(const Problem& p, const void* q, const void* k, const void* v,
-                           const void* dout, const float* lse, const float* dvec,
-                           float* dq_acc, void* dk, void* dv, cudaStream_t st);
+cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          const void* dout, const float* lse2, const float* dvec, float* dq_acc,
+                          void* dk, void* dv, int npad, cudaStream_t st);
 
 }  // namespace fa

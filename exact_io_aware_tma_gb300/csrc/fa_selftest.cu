@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(128, 1)
 
   const int b_halves = (mode == 0) ? 2 : n / 64;
   if (threadIdx.x == 0) {
-    const bool a_by_tma = (mode == 0 || mode == 1);
+    const bool a_by_tma = (mode == 0 || mode == 1 || mode == 4);
     mbar_expect_tx(bars, (a_by_tma ? 2 * kHalf : 0) + b_halves * kHalf);
     if (a_by_tma)
       for (int h = 0; h < 2; ++h) tma_load_3d(sA + h * kHalf, &tm_a, bars, h * 64, 0, 0);
@@ -81,7 +81,13 @@ __global__ void __launch_bounds__(128, 1)
   bool ok = mbar_wait(bars, 0, ab);
   if (ok && threadIdx.x == 0) {
     tc_fence_after();
-    if (mode == 0) {
+    if (mode == 4) {
+      // c = a^T b: A operand MN-major (M = columns of a, K = rows of a)
+      const uint32_t id = idesc_bf16(128, n, true, true);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem, sdesc_sw128(sA + kk * 2048, kHalf, 1024),
+               sdesc_sw128(sB + kk * 2048, kHalf, 1024), id, kk > 0);
+    } else if (mode == 0) {
       const uint32_t id = idesc_bf16(128, 128, false, false);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -123,7 +129,7 @@ using namespace fa;
 
 extern "C" int fa_selftest_mma(int mode, const void* a, const void* b, float* c, int n,
                                void* stream) {
-  if (mode < 0 || mode > 3 || !a || !b || !c) return 1;
+  if (mode < 0 || mode > 4 || !a || !b || !c) return 1;
   if (mode != 0 && n != 64 && n != 128) return 1;
   CUtensorMap ta, tb;
   if (!make_bf16_map_3d(&ta, a, 128, 128, 1, 128)) return 3;

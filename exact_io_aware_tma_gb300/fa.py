@@ -24,8 +24,8 @@ SIGNATURES = {
     "fa_forward": ([_vp] * 5 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
     "fa_backward_workspace_bytes": ([_i] * 4, _sz),
     "fa_backward": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
-    "fa_backward_preprocess": ([_vp, _vp] + [_i] * 4 + [_vp, _sz, _vp], _i),
-    "fa_backward_dkdv": ([_vp] * 7 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
+    "fa_backward_preprocess": ([_vp, _vp, _vp] + [_i] * 4 + [_vp, _sz, _vp], _i),
+    "fa_backward_dkdv": ([_vp] * 6 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_backward_dq_convert": ([_vp] + [_i] * 4 + [_f, _vp, _sz, _vp], _i),
     "fa_tile_schedule": ([_i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
     "fa_last_device_status": ([_vp], _i),

@@ -85,9 +85,10 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
                const uint8_t* block_mask, const int32_t* kv_len, void* stream);
 
 /*
- * Bytes of device workspace fa_backward needs: D (fp32 [B,H,N]) followed by
- * the fp32 dQ accumulator [B,H,N,d], each 256-byte aligned.  O(B*H*N*d):
- * linear in N (no N x N buffer).  Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_backward needs: LSE*log2(e) and D
+ * (fp32 [B*H][Np] each, Np = N rounded up to a multiple of 128) followed by
+ * the fp32 dQ accumulator [B,H,N,d], each part 256-byte aligned.
+ * O(B*H*N*d): linear in N (no N x N buffer).  Returns 0 for invalid sizes.
  */
 FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
@@ -118,21 +119,23 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
  * same workspace is exactly fa_backward.  Arguments mean what they mean in
  * fa_backward; each validates its own arguments.
  *
- * fa_backward_preprocess: D = rowsum(dO * O) into the workspace (fp32
- *   [B,H,N]) and clears the workspace's fp32 dQ accumulator [B,H,N,d].
+ * fa_backward_preprocess: D = rowsum(dO * O) and LSE*log2(e) into the
+ *   workspace (padding rows and rows without an allowed key get +inf, so
+ *   their probabilities rebuild as 0) and clears the workspace's fp32 dQ
+ *   accumulator [B,H,N,d].
  * fa_backward_dkdv: for every live 128-key tile, recomputes P and dS from
- *   Q, K, V, dO, LSE and D, writes dK (times scale) and dV, and adds dS K
- *   into the workspace's dQ accumulator.  Needs the preprocess first.
+ *   Q, K, V, dO and the workspace's LSE and D, writes dK (times scale) and
+ *   dV, and adds dS K into the workspace's dQ accumulator.  Needs the
+ *   preprocess first.
  * fa_backward_dq_convert: dQ = scale * accumulator, rounded to bf16.
  */
-FA_API int fa_backward_preprocess(const void* o, const void* dout, int B, int H, int N,
-                                  int d, void* workspace, size_t workspace_bytes,
-                                  void* stream);
-FA_API int fa_backward_dkdv(const void* q, const void* k, const void* v, const float* lse,
-                            const void* dout, void* dk, void* dv, int B, int H, int N,
-                            int d, float scale, int causal, const uint8_t* block_mask,
-                            const int32_t* kv_len, void* workspace,
-                            size_t workspace_bytes, void* stream);
+FA_API int fa_backward_preprocess(const void* o, const void* dout, const float* lse, int B,
+                                  int H, int N, int d, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+FA_API int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dout,
+                            void* dk, void* dv, int B, int H, int N, int d, float scale,
+                            int causal, const uint8_t* block_mask, const int32_t* kv_len,
+                            void* workspace, size_t workspace_bytes, void* stream);
 FA_API int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
                                   const void* workspace, size_t workspace_bytes,
                                   void* stream);

@@ -8,7 +8,7 @@
  *
  *   a : bf16 [128][128] row-major.
  *   b : mode 0: bf16 [128][128] row-major (one row per output column);
- *       modes 1-3: bf16 [128][n] row-major.
+ *       modes 1-4: bf16 [128][n] row-major.
  *   c : fp32 [128][n] row-major output (n = 128 in mode 0).
  *   mode 0: c = a * b^T  (both operands K-major in shared memory via TMA;
  *           the S = Q K^T path).
@@ -18,7 +18,10 @@
  *           MN-major via TMA; the O += P V path with P in tensor memory).
  *   mode 3: c = a * b    (a written to shared memory by threads in the
  *           128-byte-swizzled layout, b MN-major via TMA).
- *   n    : 64 or 128 (modes 1-3).
+ *   mode 4: c = a^T * b (a MN-major via TMA, i.e. the M index runs along
+ *           a's rows in memory; b MN-major via TMA; the dQ^T = K^T dS^T
+ *           path of the backward).
+ *   n    : 64 or 128 (modes 1-4).
  * Returns 0 on success, 1 on a bad argument, 3 on a CUDA error.  A bounded
  * wait that gives up is reported by fa_last_device_status().
  */

@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("mode,n", [(0, 128), (1, 64), (1, 128), (2, 64), (2, 128),
-                                    (3, 64), (3, 128)])
+                                    (3, 64), (3, 128), (4, 64), (4, 128)])
 def test_single_tile_mma(mode, n):
     g = torch.Generator().manual_seed(100 + 10 * mode + n)
     a = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
@@ -19,7 +19,12 @@ def test_single_tile_mma(mode, n):
     c = fa.selftest_mma(mode, a, b, n)
     torch.cuda.synchronize()
     assert fa.last_device_status() == fa.FA_OK
-    ref = a.double() @ (b.double().T if mode == 0 else b.double())
+    if mode == 0:
+        ref = a.double() @ b.double().T
+    elif mode == 4:
+        ref = a.double().T @ b.double()
+    else:
+        ref = a.double() @ b.double()
     err = (c.double() - ref).abs().max().item()
     # fp32 accumulation of 128 exact bf16 products
     assert err <= 1e-5 * ref.abs().max().item() * 16, (mode, n, err)
