@@ -54,6 +54,29 @@ def dense_fraction(cfg):
     return 1.0
 
 
+# ---------------------------------------------------------------- ranks
+#
+# Heads (and batches) are independent, so N GPUs run N replicas of the
+# workload, each on its own seeded inputs, with no collective in the data
+# path; the only cross-rank steps are the barriers around the timed region
+# and the max over ranks of the measured times.
+
+def rank_seed(base_seed, rank):
+    """Seed of a rank's replica: distinct per rank, rank 0 keeps the base."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value, device=None):
+    """Max of a per-rank float over the process group (identity when N=1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -219,7 +242,7 @@ def run_gpu(args, cfg, name):
 
     # The oracle sample runs before any GPU work on rank 0 (N=1 only).
     cpu_base = None
-    inp = make_inputs(**{**cfg, "seed": cfg["seed"] + rank})
+    inp = make_inputs(**{**cfg, "seed": rank_seed(cfg["seed"], rank)})
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, fl, desc = oracle_sample(inp)
         cpu_base = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
@@ -289,11 +312,7 @@ def run_gpu(args, cfg, name):
 
     seg = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(4)]
                     for i in range(args.steps)])  # ms: fwd, pre, dkdv, convert
-    step_ms = float(seg.sum(axis=1).mean())
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(float(seg.sum(axis=1).mean()), dev)
 
     frac = dense_fraction(cfg)
     f_fwd, f_bwd = flops(cfg, frac)
@@ -328,11 +347,7 @@ def run_gpu(args, cfg, name):
                 h_.copy_(d_, non_blocking=True)
             e_ev[i][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = statistics.mean(a.elapsed_time(b) for a, b in e_ev[1:])
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_ev[1:]), dev)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
         d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
         e2e = {"value": world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
