@@ -30,7 +30,11 @@ SIGNATURES = {
     "fa_tile_schedule": ([_i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
     "fa_last_device_status": ([_vp], _i),
     "fa_selftest_mma": ([_i, _vp, _vp, _vp, _i, _vp], _i),
+    "fa_backward_noalloc": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
 }
+
+# Size of the library's built-in backward scratch (include/fa.h).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class FAError(RuntimeError):
@@ -133,6 +137,29 @@ def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
                          workspace.numel() * workspace.element_size(), _stream(stream))
     if st != FA_OK:
         raise FAError(st, "fa_backward")
+    return dq, dk, dv
+
+
+def backward_noalloc(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
+                     scale=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV like ``backward`` but with no workspace: the library's
+    built-in scratch is used (``fa_backward_noalloc``; problems needing more
+    than NOALLOC_SCRATCH_BYTES of workspace are rejected).  Output tensors
+    are allocated here unless given; pass ``dq``/``dk``/``dv`` to allocate
+    nothing at all."""
+    lib = load()
+    _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    bm, kl = _mask_args(N, block_mask, kv_len, B)
+    st = lib.fa_backward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, scale,
+                                 int(bool(causal)), bm, kl, _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_backward_noalloc")
     return dq, dk, dv
 
 

@@ -141,6 +141,38 @@ FA_API int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float sc
                                   void* stream);
 
 /*
+ * Backward pass for callers that cannot allocate device memory.  (No
+ * counterpart in the method's description: an interface convenience.)
+ *
+ * Who needs it: code embedded in a host framework that owns every device
+ * allocation (its own pool or memory budget) and forbids raw cudaMalloc from
+ * plug-ins, and latency-critical callers that must keep cudaMalloc/cudaFree
+ * (which can synchronise the whole device) off their hot path -- callers
+ * that therefore cannot hand fa_backward a workspace.
+ *
+ * Same arguments and results as fa_backward, minus the workspace: the
+ * library uses a fixed array of FA_NOALLOC_SCRATCH_BYTES of device memory
+ * that is part of the library image, reserved on every GPU that loads the
+ * library and held until the process exits.  Nothing is allocated.
+ *  - Problems whose fa_backward_workspace_bytes() exceeds
+ *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_INVALID_ARG before
+ *    any CUDA call (32 MiB covers e.g. B*H*N*d up to about 8 million
+ *    elements).
+ *  - The first call on a device looks up the array's device address on that
+ *    device (the current device) and caches it; make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array.  Each call rewrites every
+ *    part of it that it reads (the dQ accumulator is cleared first), but
+ *    calls whose work overlaps on the GPU (other streams, other host
+ *    threads) race on it: serialise them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+FA_API int fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk,
+                               void* dv, int B, int H, int N, int d, float scale, int causal,
+                               const uint8_t* block_mask, const int32_t* kv_len, void* stream);
+
+/*
  * Tile schedule of one batch element, as the kernels enumerate it: every
  * live (query tile, key tile) pair of 128x128 tiles, i.e. every tile pair
  * holding at least one allowed (i, j), in query-tile-major order, with a
