@@ -58,9 +58,19 @@ struct FwdTc {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-// Next key tile after kt that is live for query tile q0 or q1 (q1 < 0: absent).
+// Last key tile of the union of live tiles of query tiles q0 and q1 (q1 < 0:
+// absent) when there is no block mask: the live tiles are then exactly
+// 0..last (key limit, and the causal rule kt <= qt).
+__device__ __forceinline__ int union_last(const Problem& p, int q0, int q1, int klim) {
+  int last = klim > 0 ? (klim - 1) / kTile : -1;
+  if (p.causal) last = min(last, max(q0, q1));
+  return last;
+}
+
+// Next key tile after kt that is live for query tile q0 or q1.
 __device__ __forceinline__ int next_union_tile(const Problem& p, int q0, int q1, int klim,
-                                               int kt) {
+                                               int last, int kt) {
+  if (p.block_mask == nullptr) return kt + 1 <= last ? kt + 1 : p.T;
   for (++kt; kt < p.T; ++kt)
     if (tile_live(p, q0, kt, klim) || (q1 >= 0 && tile_live(p, q1, kt, klim))) return kt;
   return p.T;
@@ -90,6 +100,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   const int qt0 = 2 * pair;
   const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
   const int klim = key_limit(p, b);
+  const int ulast = union_last(p, qt0, qt1, klim);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i)
@@ -125,8 +136,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
       bool ok = true;
-      for (int kt = next_union_tile(p, qt0, qt1, klim, -1); kt < p.T && ok;
-           kt = next_union_tile(p, qt0, qt1, klim, kt)) {
+      for (int kt = next_union_tile(p, qt0, qt1, klim, ulast, -1); kt < p.T && ok;
+           kt = next_union_tile(p, qt0, qt1, klim, ulast, kt)) {
         for (int which = 0; which < 2; ++which) {
           if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) {
             ok = false;
@@ -164,100 +175,84 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Kept lean: one thread issues every GEMM as a single instruction
+    // sequence from precomputed descriptors, so the tensor core is not left
+    // waiting on this thread's bookkeeping.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
-      const uint32_t q_s[2] = {s0 + C::OFF_Q, s0 + C::OFF_Q + C::TILE};
-      const uint32_t col_s[2] = {C::COL_S0, C::COL_S1};
-      const uint32_t col_o[2] = {C::COL_O0, C::COL_O1};
-      auto issue_qk = [&](int i, uint32_t kslot) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32;
-          mma_ss(tmem + col_s[i], sdesc_sw128(q_s[i] + off, 16, 1024),
-                 sdesc_sw128(kslot + off, 16, 1024), id_qk, kk > 0);
-        }
+      constexpr uint32_t slot_step = C::TILE >> 4;  // descriptor units per ring slot
+      const uint64_t dq0 = sdesc_sw128(s0 + C::OFF_Q, 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(s0 + C::OFF_Q + C::TILE, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(s0 + C::OFF_KV, 16, 1024);      // K operand of slot 0
+      const uint64_t dv0 = sdesc_sw128(s0 + C::OFF_KV, C::HALF, 1024);  // V operand of slot 0
+      const uint32_t t_s0 = tmem + C::COL_S0, t_s1 = tmem + C::COL_S1;
+      const uint32_t t_o0 = tmem + C::COL_O0, t_o1 = tmem + C::COL_O1;
+      auto qk = [&](uint32_t t_s, uint64_t dq, int slot) {
+        if (D == 128)
+          mma_ss_kmajor_k128_h16k(t_s, dq, dk0 + (uint64_t)(slot * slot_step), id_qk, 0);
+        else
+          mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)(slot * slot_step), id_qk, 0);
       };
-      auto issue_pv = [&](int i, uint32_t vslot, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + col_o[i], tmem + col_s[i] + kk * 8,
-                 sdesc_sw128(vslot + kk * 2048, C::HALF, 1024), id_pv, acc || kk > 0);
-      };
-      int slot = 0, round = 0;
-      auto take = [&](uint32_t& addr, int& bslot, int& par) {
-        addr = s0 + C::OFF_KV + slot * C::TILE;
-        bslot = slot;
-        par = round & 1;
-        if (++slot == C::NSLOT) {
-          slot = 0;
-          ++round;
-        }
-      };
+      int slot = 0, phase = 0;  // next ring slot to consume and its phase parity
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
-      int cur = next_union_tile(p, qt0, qt1, klim, -1);
-      int npv[2] = {0, 0};
-      uint32_t kaddr;
-      int kslot, kpar;
+      int cur = next_union_tile(p, qt0, qt1, klim, ulast, -1);
+      int npv0 = 0, npv1 = 0;
       if (ok && cur < p.T) {
-        take(kaddr, kslot, kpar);
-        ok = mbar_wait(bar(C::B_FULL + kslot), kpar, ab);
+        ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
         tc_fence_after();
         if (ok) {
           if (tile_live(p, qt0, cur, klim)) {
-            issue_qk(0, kaddr);
+            qk(t_s0, dq0, slot);
             mma_commit(bar(C::B_S + 0));
           }
           if (qt1 >= 0 && tile_live(p, qt1, cur, klim)) {
-            issue_qk(1, kaddr);
+            qk(t_s1, dq1, slot);
             mma_commit(bar(C::B_S + 1));
           }
-          mma_commit(bar(C::B_EMPTY + kslot));
+          mma_commit(bar(C::B_EMPTY + slot));
         }
+        if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
       }
       while (ok && cur < p.T) {
         const bool l0 = tile_live(p, qt0, cur, klim);
         const bool l1 = qt1 >= 0 && tile_live(p, qt1, cur, klim);
-        uint32_t vaddr;
-        int vslot, vpar;
-        take(vaddr, vslot, vpar);
-        const int nxt = next_union_tile(p, qt0, qt1, klim, cur);
+        const int vslot = slot, vphase = phase;
+        if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
+        const int nxt = next_union_tile(p, qt0, qt1, klim, ulast, cur);
         const bool has_next = nxt < p.T;
         const bool n0 = has_next && tile_live(p, qt0, nxt, klim);
         const bool n1 = has_next && qt1 >= 0 && tile_live(p, qt1, nxt, klim);
-        uint32_t naddr = 0;
-        int nslot = 0, npar = 0;
-        if (has_next) take(naddr, nslot, npar);
-        if (!(ok = mbar_wait(bar(C::B_FULL + vslot), vpar, ab))) break;
+        const int kslot = slot, kphase = phase;
+        if (has_next && ++slot == C::NSLOT) { slot = 0; phase ^= 1; }
+        const uint64_t dv = dv0 + (uint64_t)(vslot * slot_step);
+        if (!(ok = mbar_wait(bar(C::B_FULL + vslot), vphase, ab))) break;
+        if (has_next && !(ok = mbar_wait(bar(C::B_FULL + kslot), kphase, ab))) break;
         tc_fence_after();
         if (l0) {
-          if (!(ok = mbar_wait(bar(C::B_P + 0), npv[0] & 1, ab))) break;
+          if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
           tc_fence_after();
-          issue_pv(0, vaddr, npv[0] > 0);
-          ++npv[0];
+          mma_ts_mn_k128(t_o0, t_s0, dv, id_pv, npv0 > 0);
+          ++npv0;
         }
-        if (has_next) {
-          if (!(ok = mbar_wait(bar(C::B_FULL + nslot), npar, ab))) break;
-          tc_fence_after();
-          if (n0) {
-            issue_qk(0, naddr);
-            mma_commit(bar(C::B_S + 0));
-          }
+        if (n0) {
+          qk(t_s0, dq0, kslot);
+          mma_commit(bar(C::B_S + 0));
         }
         if (l1) {
-          if (!(ok = mbar_wait(bar(C::B_P + 1), npv[1] & 1, ab))) break;
+          if (!(ok = mbar_wait(bar(C::B_P + 1), npv1 & 1, ab))) break;
           tc_fence_after();
-          issue_pv(1, vaddr, npv[1] > 0);
-          ++npv[1];
+          mma_ts_mn_k128(t_o1, t_s1, dv, id_pv, npv1 > 0);
+          ++npv1;
         }
         mma_commit(bar(C::B_EMPTY + vslot));
         if (has_next) {
           if (n1) {
-            issue_qk(1, naddr);
+            qk(t_s1, dq1, kslot);
             mma_commit(bar(C::B_S + 1));
           }
-          mma_commit(bar(C::B_EMPTY + nslot));
+          mma_commit(bar(C::B_EMPTY + kslot));
         }
         cur = nxt;
       }
@@ -283,18 +278,17 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       float m_ref = -INFINITY, l = 0.f;
       int n = 0;
       bool ok = true;
-      for (int kt = next_union_tile(p, qt0, qt1, klim, -1); kt < p.T;
-           kt = next_union_tile(p, qt0, qt1, klim, kt)) {
+      for (int kt = next_union_tile(p, qt0, qt1, klim, ulast, -1); kt < p.T;
+           kt = next_union_tile(p, qt0, qt1, klim, ulast, kt)) {
         if (!tile_live(p, qt, kt, klim)) continue;
         if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
         tc_fence_after();
         float s[128];
+        {
+          uint32_t raw[128];
+          tmem_ld128(lane_base + col_s, raw);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t raw[32];
-          tmem_ld32(lane_base + col_s + 32 * c, raw);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]);
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(raw[c]);
         }
         const bool diag = p.causal && kt == qt;
         if (diag || (kt + 1) * 128 > klim) {
@@ -304,14 +298,25 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= lim) s[c] = -INFINITY;
         }
-        float mx = -INFINITY;
+        // row max (row min for a negative scale): 4 independent chains of
+        // 3-input max
+        float mx;
         if (cl2 >= 0.f) {
+          // s[0..3] seed the chains; 15 steps cover s[4..123]; s[124..127] last
+          float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+          for (int c = 4; c + 8 <= 124; c += 8)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m4[e] = max3f(m4[e], s[c + e], s[c + 4 + e]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(m4[e], s[124 + e]);
+          mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         } else {
-          float mn = INFINITY;
+          float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mn = fminf(mn, s[c] == -INFINITY ? INFINITY : s[c]);
+          for (int c = 0; c < 128; ++c)
+            m4[c & 3] = fminf(m4[c & 3], s[c] == -INFINITY ? INFINITY : s[c]);
+          const float mn = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
           mx = mn == INFINITY ? -INFINITY : mn;
         }
         const float m_tile = mx == -INFINITY ? -INFINITY : mx * cl2;
@@ -320,20 +325,25 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
           alpha = fast_exp2(m_ref - m_tile);  // 0 when m_ref = -inf
           m_ref = m_tile;
         }
-        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-        float sum = 0.f;
+        const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
+        // p = 2^(s * scale*log2e - m): argument by packed FMA, exp2 on MUFU,
+        // row sum by packed adds over four independent pairs
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float p0 = fast_exp2(fmaf(s[32 * c + 2 * j], cl2, -ref));
-            const float p1 = fast_exp2(fmaf(s[32 * c + 2 * j + 1], cl2, -ref));
-            sum += p0 + p1;
+            float x0, x1;
+            fma2(x0, x1, s[32 * c + 2 * j], s[32 * c + 2 * j + 1], cl2, cl2, nref, nref);
+            const float p0 = fast_exp2(x0);
+            const float p1 = fast_exp2(x1);
+            add2(sa[j & 3], sb[j & 3], sa[j & 3], sb[j & 3], p0, p1);
             pk[j] = pack_bf16(p0, p1);
           }
           tmem_st16(lane_base + col_s + 16 * c, pk);
         }
+        const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
         l = l * alpha + sum;
         if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll

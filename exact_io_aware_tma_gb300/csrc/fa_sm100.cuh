@@ -197,6 +197,77 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+
+// ---- GEMMs issued as one instruction sequence each (descriptor offsets
+// folded into immediates; the first MMA honours `acc`, the rest accumulate).
+
+// K = 128 (8 MMAs), both operands K-major in 16 KB column halves.
+__device__ __forceinline__ void mma_ss_kmajor_k128_h16k(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                      uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b64 a, b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      " add.s64 a, %1, 2;\n add.s64 b, %2, 2;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 4;\n add.s64 b, %2, 4;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 6;\n add.s64 b, %2, 6;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1024;\n add.s64 b, %2, 1024;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1026;\n add.s64 b, %2, 1026;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1028;\n add.s64 b, %2, 1028;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1030;\n add.s64 b, %2, 1030;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      "}\n" ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+// K = 64 (4 MMAs), both operands K-major (one 64-column half).
+__device__ __forceinline__ void mma_ss_kmajor_k64(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                      uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b64 a, b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      " add.s64 a, %1, 2;\n add.s64 b, %2, 2;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 4;\n add.s64 b, %2, 4;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 6;\n add.s64 b, %2, 6;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      "}\n" ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+// K = 128 (8 MMAs): A from TMEM (8 columns per K step), B MN-major (16 rows = 2048 B per step).
+__device__ __forceinline__ void mma_ts_mn_k128(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                      uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b32 a;\n .reg .b64 b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " add.u32 a, %1, 8;\n add.s64 b, %2, 128;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 16;\n add.s64 b, %2, 256;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 24;\n add.s64 b, %2, 384;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 32;\n add.s64 b, %2, 512;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 40;\n add.s64 b, %2, 640;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 48;\n add.s64 b, %2, 768;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 56;\n add.s64 b, %2, 896;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      "}\n" ::"r"(d), "r"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
 // TMEM -> registers: 32 lanes x 32 consecutive 32-bit columns; thread t of
 // the warp receives lane (warp's lane base + t).  Waits for completion.
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
@@ -212,6 +283,59 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 #undef FA_R8
+
+
+// TMEM -> registers, 32 lanes x 128 consecutive columns in one instruction,
+// then one completion wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+}
+
+// TMEM -> registers: 32 lanes x 64 columns, one completion wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+// TMEM -> registers: two blocks of 32 lanes x 32 columns, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(a0), "r"(a1)
+      : "memory");
+}
+
+// ---- packed fp32 arithmetic (two lanes per instruction) and 3-input max
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n .reg .b64 x, y, z, w;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " mov.b64 z, {%6, %7};\n fma.rn.f32x2 w, x, y, z;\n mov.b64 {%0, %1}, w;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 x, y, w;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " add.rn.f32x2 w, x, y;\n mov.b64 {%0, %1}, w;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 #define FA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                  "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
