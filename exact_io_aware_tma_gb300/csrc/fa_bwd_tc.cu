@@ -72,7 +72,9 @@ struct BwdTc {
 };
 
 // Next 64-row query step after (qt, sub) for key tile kt: live query tiles
-// in ascending order, two halves each, skipping halves past N.
+// in ascending order, two halves each, skipping halves past N.  Without a
+// block mask the live query tiles are contiguous (causal: from kt on), so the
+// first one is found in closed form.
 __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, int& qt,
                                             int& sub) {
   if (qt >= 0 && sub == 0 && qt * 128 + 64 < p.N) {
@@ -80,6 +82,11 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, 
     return true;
   }
   sub = 0;
+  if (p.block_mask == nullptr) {
+    if (kt * kTile >= klim) return false;  // dead key tile
+    qt = qt < 0 ? (p.causal ? kt : 0) : qt + 1;
+    return qt < p.T;
+  }
   for (++qt; qt < p.T; ++qt)
     if (tile_live(p, qt, kt, klim)) return true;
   return false;
@@ -177,38 +184,40 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Kept lean like the forward's: each GEMM is one instruction sequence
+    // from precomputed descriptors.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, C::BQ, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
       constexpr uint32_t id_q = idesc_bf16(128, C::BQ, true, true);
-      const uint32_t sK = s0 + C::OFF_K, sV = s0 + C::OFF_V;
-      auto stage_addr = [&](int i) { return s0 + C::OFF_ST + (i % C::NS) * C::STAGE; };
+      constexpr uint32_t st_step = C::STAGE >> 4, qb_step = C::QB >> 4, ds_step = C::DS >> 4;
+      const uint64_t dk_k = sdesc_sw128(s0 + C::OFF_K, 16, 1024);       // K, K-major
+      const uint64_t dv_k = sdesc_sw128(s0 + C::OFF_V, 16, 1024);       // V, K-major
+      const uint64_t dk_mn = sdesc_sw128(s0 + C::OFF_K, C::HALF_K, 1024);  // K^T, MN-major
+      const uint64_t dst_k = sdesc_sw128(s0 + C::OFF_ST, 16, 1024);     // stage 0 Q, K-major
+      const uint64_t dst_mn = sdesc_sw128(s0 + C::OFF_ST, C::HALF_Q, 1024);  // stage 0 Q, MN-major
+      const uint64_t dds = sdesc_sw128(s0 + C::OFF_DS, 16, 1024);       // dS^T buffer 0
+      const uint32_t t_dv = tmem + C::COL_DV, t_dk = tmem + C::COL_DK;
       bool ok = mbar_wait(bar(C::B_KV), 0, ab);
       tc_fence_after();
       // S^T and dP^T of step j into buffer j % 2.
       auto issue_sdp = [&](int j) -> bool {
         const int bf = j & 1;
-        const uint32_t st = stage_addr(j);
+        const uint64_t sq = dst_k + (uint64_t)((j % C::NS) * st_step);
         if (!mbar_wait(bar(C::B_FULL + j % C::NS), (j / C::NS) & 1, ab)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * C::HALF_K + (kk & 3) * 32;
-          const uint32_t qa = (kk >> 2) * C::HALF_Q + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + 64 * bf, sdesc_sw128(sK + ka, 16, 1024),
-                 sdesc_sw128(st + qa, 16, 1024), id_s, kk > 0);
-        }
+        if (D == 128)
+          mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
+        else
+          mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
         if (j >= 2) {
           if (!mbar_wait(bar(C::B_DQE + bf), ((j - 2) >> 1) & 1, ab)) return false;
           tc_fence_after();
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * C::HALF_K + (kk & 3) * 32;
-          const uint32_t qa = (kk >> 2) * C::HALF_Q + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_DP + 64 * bf, sdesc_sw128(sV + ka, 16, 1024),
-                 sdesc_sw128(st + C::QB + qa, 16, 1024), id_s, kk > 0);
-        }
+        if (D == 128)
+          mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
+        else
+          mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
         mma_commit(bar(C::B_S + bf));
         return true;
       };
@@ -221,26 +230,17 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       int qi_t = -1, qi_s = 0;
       for (int i = 0; ok && next_q_step(p, kt, klim, qi_t, qi_s); ++i) {
         const int bf = i & 1;
-        const uint32_t st = stage_addr(i);
+        const uint64_t sq_mn = dst_mn + (uint64_t)((i % C::NS) * st_step);
+        const uint64_t ds = dds + (uint64_t)(bf * ds_step);
         if (!(ok = mbar_wait(bar(C::B_EW + bf), (i >> 1) & 1, ab))) break;
         tc_fence_after();
-        // dV += P^T dO   (P^T: bf16 in TMEM over S[bf])
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 64 * bf + kk * 8,
-                 sdesc_sw128(st + C::QB + kk * 2048, C::HALF_Q, 1024), id_kv, (i > 0) || (kk > 0));
+        // dV += P^T dO   (P^T: bf16 in TMEM over S[bf]; dO as MN-major B)
+        mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
         // dK += dS^T Q
-        const uint32_t ds = s0 + C::OFF_DS + bf * C::DS;
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ss(tmem + C::COL_DK, sdesc_sw128(ds + kk * 32, 16, 1024),
-                 sdesc_sw128(st + kk * 2048, C::HALF_Q, 1024), id_kv, (i > 0) || (kk > 0));
+        mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, i > 0);
         mma_commit(bar(C::B_EMPTY + i % C::NS));
         // dQ^T = K^T dS^T over dP[bf]
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::COL_DP + 64 * bf, sdesc_sw128(sK + kk * 2048, C::HALF_K, 1024),
-                 sdesc_sw128(ds + kk * 2048, 16, 1024), id_q, kk > 0);
+        mma_ss_mn_mn_k128(tmem + C::COL_DP + 64 * bf, dk_mn, ds, id_q, 0);
         mma_commit(bar(C::B_DQF + bf));
         if (next_q_step(p, kt, klim, qa_t, qa_s)) {
           if (!(ok = issue_sdp(issued))) break;
@@ -270,10 +270,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       if (!(ok = mbar_wait(bar(C::B_S + bf), (i >> 1) & 1, ab))) break;
       tc_fence_after();
       uint32_t sr[64], pr[64];
-      tmem_ld32(lane_base + C::COL_S + 64 * bf, sr);
-      tmem_ld32(lane_base + C::COL_S + 64 * bf + 32, sr + 32);
-      tmem_ld32(lane_base + C::COL_DP + 64 * bf, pr);
-      tmem_ld32(lane_base + C::COL_DP + 64 * bf + 32, pr + 32);
+      tmem_ld64(lane_base + C::COL_S + 64 * bf, sr);
+      tmem_ld64(lane_base + C::COL_DP + 64 * bf, pr);
       // queries c allowed for this key: c >= lo (causal) and key < klim
       int lo = 0;
       if (j >= klim) lo = 64;
@@ -371,10 +369,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab))) break;
       tc_fence_after();
       uint32_t v[64];
-      if (valid) {
-        tmem_ld32(lane_base + C::COL_DP + 64 * bf, v);
-        tmem_ld32(lane_base + C::COL_DP + 64 * bf + 32, v + 32);
-      }
+      if (valid) tmem_ld64(lane_base + C::COL_DP + 64 * bf, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_DQE + bf));
