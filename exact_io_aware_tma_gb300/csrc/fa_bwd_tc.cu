@@ -13,9 +13,9 @@
 //     dS^T = P^T * (dP^T - D)                    (bf16 to shared memory)
 //     dV  += P^T dO             (A = P^T from TMEM)
 //     dK  += dS^T Q             (scaled by `scale` in the epilogue)
-//     dQ^T = K^T dS^T           (TMEM, d x 64; reduce-added into the fp32 dQ
-//                                accumulator by a TMA reduce; the conversion
-//                                kernel applies `scale`)
+//     dQ^T = K^T dS^T           (TMEM, d x 64; added into the fp32 dQ
+//                                accumulator; the conversion kernel
+//                                applies `scale`)
 // with D = rowsum(dO * O) and LSE*log2e precomputed per query row.
 //
 // Warp roles (384 threads):
@@ -24,8 +24,9 @@
 //   warp 1      MMA issuer (one thread); owns TMEM.
 //   warps 4-7   element-wise: P^T, dS^T (one key row per thread); at the
 //               end dK, dV from TMEM to bf16 and a TMA store.
-//   warps 8-11  dQ: dQ^T from TMEM (one head-dim row per thread) to shared
-//               memory, then TMA reduce-adds of two 32 x d fp32 tiles.
+//   warps 8-11  dQ: dQ^T from TMEM (one head-dim row per thread), added into
+//               the fp32 accumulator with red.global.add (coalesced across
+//               the warp), so the dQ tile costs no shared-memory traffic.
 //
 // TMEM columns: dV [0,d), dK [d,2d), S[b] = 2d + 64b, dP[b] = 2d + 128 + 64b
 // for the two step buffers b; dQ^T of step i is written over dP[i % 2] once
@@ -56,10 +57,7 @@ struct BwdTc {
   static constexpr int OFF_VEC = OFF_ST + NS * STAGE;  // [NS][LSE*log2e (64), D (64)]
   static constexpr int OFF_DS = (OFF_VEC + NS * 512 + 1023) / 1024 * 1024;
   static constexpr int DS = 128 * BQ * 2;             // dS^T [128 keys][64 q] bf16, x2
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS;      // fp32 [32 q][D] staging
-  static constexpr int DQ_ROWS = 32;                  // dQ reduce-add box height
-  static constexpr int DQB = DQ_ROWS * D * 4;
-  static constexpr int OFF_BAR = OFF_DQ + DQB;
+  static constexpr int OFF_BAR = OFF_DS + 2 * DS;
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_S = 1 + 2 * NS, B_EW = B_S + 2,
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_FIN = B_DQE + 2,
                        B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 1;
@@ -97,8 +95,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                  const __grid_constant__ CUtensorMap tm_dq, Problem p,
-                  const float* __restrict__ lse2, const float* __restrict__ dvec, int npad) {
+                  Problem p, const float* __restrict__ lse2, const float* __restrict__ dvec,
+                  float* __restrict__ dq_acc, int npad) {
   using C = BwdTc<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -133,7 +131,6 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_do);
-    prefetch_tensormap(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -281,21 +278,26 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 L = reinterpret_cast<const float4*>(l2)[c4];
         const float4 Dd = reinterpret_cast<const float4*>(dv)[c4];
-        const float lv[4] = {L.x, L.y, L.z, L.w};
-        const float dd[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
-        float pv[4], dsv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          float pe = fast_exp2(fmaf(__uint_as_float(sr[c]), cl2, -lv[e]));
-          if (c < lo) pe = 0.f;
-          pv[e] = pe;
-          dsv[e] = pe * (__uint_as_float(pr[c]) - dd[e]);
+        float x0, x1, x2, x3;
+        fma2(x0, x1, __uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1]), cl2, cl2, -L.x,
+             -L.y);
+        fma2(x2, x3, __uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3]), cl2, cl2,
+             -L.z, -L.w);
+        float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+        if (lo > 0) {
+          const int c = 4 * c4;
+          if (c < lo) p0 = 0.f;
+          if (c + 1 < lo) p1 = 0.f;
+          if (c + 2 < lo) p2 = 0.f;
+          if (c + 3 < lo) p3 = 0.f;
         }
-        pk[2 * c4] = pack_bf16(pv[0], pv[1]);
-        pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
-        dk[2 * c4] = pack_bf16(dsv[0], dsv[1]);
-        dk[2 * c4 + 1] = pack_bf16(dsv[2], dsv[3]);
+        float e0, e1, e2, e3;
+        add2(e0, e1, __uint_as_float(pr[4 * c4]), __uint_as_float(pr[4 * c4 + 1]), -Dd.x, -Dd.y);
+        add2(e2, e3, __uint_as_float(pr[4 * c4 + 2]), __uint_as_float(pr[4 * c4 + 3]), -Dd.z, -Dd.w);
+        pk[2 * c4] = pack_bf16(p0, p1);
+        pk[2 * c4 + 1] = pack_bf16(p2, p3);
+        dk[2 * c4] = pack_bf16(p0 * e0, p1 * e1);
+        dk[2 * c4 + 1] = pack_bf16(p2 * e2, p3 * e3);
       }
       tmem_st32(lane_base + C::COL_S + 64 * bf, pk);
       // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of
@@ -359,8 +361,6 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const int c = ((warp & 3) << 5) + lane;  // head-dim index = TMEM lane
     const bool valid = c < D;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int t = threadIdx.x - 256;  // 0..127 within the warpgroup
-    float* stg = reinterpret_cast<float*>(smem + C::OFF_DQ);
     int qt = -1, sub = 0;
     bool ok = true;
     for (int i = 0; next_q_step(p, kt, klim, qt, sub); ++i) {
@@ -373,25 +373,16 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_DQE + bf));
+      // Reduce into the fp32 accumulator straight from registers: for each
+      // query the warp's 32 lanes add 32 consecutive floats of its row.
+      if (valid) {
+        const int rows = min(64, p.N - q0);
+        float* dst = dq_acc + ((size_t)bh * p.N + q0) * D + c;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        // the staging tile is free once the previous reduce has read it
-        if (t == 0 && (i > 0 || hh > 0)) tma_store_wait_read();
-        named_barrier(2, 128);
-        if (valid) {
-#pragma unroll
-          for (int q = 0; q < C::DQ_ROWS; ++q)
-            stg[q * D + c] = __uint_as_float(v[hh * C::DQ_ROWS + q]);
-        }
-        fence_proxy_async_smem();
-        named_barrier(2, 128);
-        if (t == 0) {
-          tma_reduce_add_3d(&tm_dq, smem_u32(stg), 0, q0 + hh * C::DQ_ROWS, (int)bh);
-          tma_store_commit();
-        }
+        for (int q = 0; q < 64; ++q)
+          if (q < rows) atomicAdd(dst + (size_t)q * D, __uint_as_float(v[q]));
       }
     }
-    if (t == 0) tma_store_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -407,19 +398,18 @@ static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* 
                                    float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
   using C = BwdTc<D>;
   const long long bh = (long long)p.B * p.H;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) || !make_bf16_map_3d(&tk, k, D, p.N, bh, 128) ||
       !make_bf16_map_3d(&tv, v, D, p.N, bh, 128) ||
       !make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) ||
-      !make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) || !make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128) ||
-      !make_f32_map_3d(&tdq, dq_acc, D, p.N, bh, C::DQ_ROWS))
+      !make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) || !make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128))
     return cudaErrorInvalidValue;
   auto kern = bwd_tc_kernel<D>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)bh, (unsigned)p.T);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, lse2, dvec, npad);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad);
   return cudaGetLastError();
 }
 

@@ -372,6 +372,59 @@ __device__ __forceinline__ void mma_ss_mn_mn_k128(uint32_t d, uint64_t a, uint64
       : "memory");
 }
 
+
+// ---- backward GEMM patterns with 128-query steps
+
+// K = 128 (8 MMAs): A from TMEM with its two 64-wide K halves 64 columns apart, B MN-major.
+__device__ __forceinline__ void mma_ts_split_mn_k128(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                      uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b32 a;\n .reg .b64 b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " add.u32 a, %1, 8;\n add.s64 b, %2, 128;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 16;\n add.s64 b, %2, 256;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 24;\n add.s64 b, %2, 384;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 64;\n add.s64 b, %2, 512;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 72;\n add.s64 b, %2, 640;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 80;\n add.s64 b, %2, 768;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 88;\n add.s64 b, %2, 896;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      "}\n" ::"r"(d), "r"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+// K = 128 (8 MMAs): A K-major in 16 KB halves, B MN-major.
+__device__ __forceinline__ void mma_ss_kmajor_mn_k128(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                      uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b64 a, b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      " add.s64 a, %1, 2;\n add.s64 b, %2, 128;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 4;\n add.s64 b, %2, 256;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 6;\n add.s64 b, %2, 384;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1024;\n add.s64 b, %2, 512;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1026;\n add.s64 b, %2, 640;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1028;\n add.s64 b, %2, 768;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      " add.s64 a, %1, 1030;\n add.s64 b, %2, 896;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
+      "}\n" ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
 // TMEM -> registers: 32 lanes x 32 consecutive 32-bit columns; thread t of
 // the warp receives lane (warp's lane base + t).  Waits for completion.
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
@@ -419,6 +472,17 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t* 
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(a0), "r"(a1)
       : "memory");
+}
+
+// Read-only 16-byte global load kept at its place in the instruction stream
+// (so the compiler does not hoist a batch of them and raise register
+// pressure).
+__device__ __forceinline__ float4 ldg_f4_inplace(const float4* ptr) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr));
+  return v;
 }
 
 // ---- packed fp32 arithmetic (two lanes per instruction) and 3-input max
