@@ -218,14 +218,12 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
         mma_commit(bar(C::B_S + bf));
         return true;
       };
-      int qa_t = -1, qa_s = 0;  // iterator for the S/dP lookahead
-      int issued = 0;
-      for (int w = 0; w < 2 && ok && next_q_step(p, kt, klim, qa_t, qa_s); ++w) {
-        ok = issue_sdp(issued);
-        ++issued;
-      }
-      int qi_t = -1, qi_s = 0;
-      for (int i = 0; ok && next_q_step(p, kt, klim, qi_t, qi_s); ++i) {
+      // The issuer needs only the number of steps (descriptors depend on the
+      // step index alone), so the walk is counted once up front.
+      int nsteps = 0;
+      for (int qt = -1, sub = 0; next_q_step(p, kt, klim, qt, sub);) ++nsteps;
+      for (int j = 0; j < 2 && j < nsteps && ok; ++j) ok = issue_sdp(j);
+      for (int i = 0; ok && i < nsteps; ++i) {
         const int bf = i & 1;
         const uint64_t sq_mn = dst_mn + (uint64_t)((i % C::NS) * st_step);
         const uint64_t ds = dds + (uint64_t)(bf * ds_step);
@@ -239,10 +237,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
         // dQ^T = K^T dS^T over dP[bf]
         mma_ss_mn_mn_k128(tmem + C::COL_DP + 64 * bf, dk_mn, ds, id_q, 0);
         mma_commit(bar(C::B_DQF + bf));
-        if (next_q_step(p, kt, klim, qa_t, qa_s)) {
-          if (!(ok = issue_sdp(issued))) break;
-          ++issued;
-        }
+        if (i + 2 < nsteps && !(ok = issue_sdp(i + 2))) break;
       }
       mma_commit(bar(C::B_FIN));
       mma_commit(bar(C::B_DRAIN));

@@ -194,6 +194,15 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         else
           mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)(slot * slot_step), id_qk, 0);
       };
+      // Liveness of key tile kt for query tile 0 / 1: without a block mask
+      // it is kt <= last_i, so the loop needs no predicate calls.
+      const bool masked = p.block_mask != nullptr;
+      const int last0 = union_last(p, qt0, -1, klim);
+      const int last1 = qt1 >= 0 ? union_last(p, qt1, -1, klim) : -1;
+      auto live0 = [&](int kt) { return masked ? tile_live(p, qt0, kt, klim) : kt <= last0; };
+      auto live1 = [&](int kt) {
+        return masked ? (qt1 >= 0 && tile_live(p, qt1, kt, klim)) : kt <= last1;
+      };
       int slot = 0, phase = 0;  // next ring slot to consume and its phase parity
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
@@ -203,11 +212,11 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
         tc_fence_after();
         if (ok) {
-          if (tile_live(p, qt0, cur, klim)) {
+          if (live0(cur)) {
             qk(t_s0, dq0, slot);
             mma_commit(bar(C::B_S + 0));
           }
-          if (qt1 >= 0 && tile_live(p, qt1, cur, klim)) {
+          if (live1(cur)) {
             qk(t_s1, dq1, slot);
             mma_commit(bar(C::B_S + 1));
           }
@@ -216,14 +225,14 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
       }
       while (ok && cur < p.T) {
-        const bool l0 = tile_live(p, qt0, cur, klim);
-        const bool l1 = qt1 >= 0 && tile_live(p, qt1, cur, klim);
+        const bool l0 = live0(cur);
+        const bool l1 = live1(cur);
         const int vslot = slot, vphase = phase;
         if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
         const int nxt = next_union_tile(p, qt0, qt1, klim, ulast, cur);
         const bool has_next = nxt < p.T;
-        const bool n0 = has_next && tile_live(p, qt0, nxt, klim);
-        const bool n1 = has_next && qt1 >= 0 && tile_live(p, qt1, nxt, klim);
+        const bool n0 = has_next && live0(nxt);
+        const bool n1 = has_next && live1(nxt);
         const int kslot = slot, kphase = phase;
         if (has_next && ++slot == C::NSLOT) { slot = 0; phase ^= 1; }
         const uint64_t dv = dv0 + (uint64_t)(vslot * slot_step);
