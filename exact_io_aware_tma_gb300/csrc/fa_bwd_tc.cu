@@ -21,7 +21,9 @@
 // Warp roles (384 threads):
 //   warp 0      TMA producer: K, V once; per step Q, dO (64 rows) and the
 //               64 LSE / D values into a ring of stages.
-//   warp 1      MMA issuer (one thread); owns TMEM.
+//   warps 1, 2  MMA issuers (one thread each): warp 1 the recompute GEMMs
+//               S^T, dP^T (and owns TMEM), warp 2 the gradient GEMMs dV, dK,
+//               dQ^T.
 //   warps 4-7   element-wise: P^T, dS^T (one key row per thread); at the
 //               end dK, dV from TMEM to bf16 and a TMA store.
 //   warps 8-11  dQ: dQ^T from TMEM (one head-dim row per thread), added into
@@ -59,8 +61,8 @@ struct BwdTc {
   static constexpr int DS = 128 * BQ * 2;             // dS^T [128 keys][64 q] bf16, x2
   static constexpr int OFF_BAR = OFF_DS + 2 * DS;
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_S = 1 + 2 * NS, B_EW = B_S + 2,
-                       B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_FIN = B_DQE + 2,
-                       B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 1;
+                       B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
+                       B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;
   static constexpr int COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
@@ -179,10 +181,15 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       while (!mbar_try_wait(bar(C::B_KV), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Kept lean like the forward's: each GEMM is one instruction sequence
-    // from precomputed descriptors.
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads: issuing one tcgen05.mma costs a thread about as
+    // long as a narrow MMA takes to run, so one thread cannot feed the tensor
+    // core with all five GEMMs of a step and its barrier polls.
+    //   warp 1: S^T(j), dP^T(j) into buffer j % 2 (owns TMEM);
+    //   warp 2: dV(i), dK(i), dQ^T(i) over dP[i % 2].
+    // S^T(j) waits until dV(j-2) has read P^T(j-2) from the same columns
+    // (s_free), dP^T(j) until the dQ warps have read dQ^T(j-2) out.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, C::BQ, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
@@ -195,54 +202,57 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       const uint64_t dst_mn = sdesc_sw128(s0 + C::OFF_ST, C::HALF_Q, 1024);  // stage 0 Q, MN-major
       const uint64_t dds = sdesc_sw128(s0 + C::OFF_DS, 16, 1024);       // dS^T buffer 0
       const uint32_t t_dv = tmem + C::COL_DV, t_dk = tmem + C::COL_DK;
-      bool ok = mbar_wait(bar(C::B_KV), 0, ab);
-      tc_fence_after();
-      // S^T and dP^T of step j into buffer j % 2.
-      auto issue_sdp = [&](int j) -> bool {
-        const int bf = j & 1;
-        const uint64_t sq = dst_k + (uint64_t)((j % C::NS) * st_step);
-        if (!mbar_wait(bar(C::B_FULL + j % C::NS), (j / C::NS) & 1, ab)) return false;
-        tc_fence_after();
-        if (D == 128)
-          mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
-        else
-          mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
-        if (j >= 2) {
-          if (!mbar_wait(bar(C::B_DQE + bf), ((j - 2) >> 1) & 1, ab)) return false;
-          tc_fence_after();
-        }
-        if (D == 128)
-          mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
-        else
-          mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
-        mma_commit(bar(C::B_S + bf));
-        return true;
-      };
-      // The issuer needs only the number of steps (descriptors depend on the
+      // The issuers need only the number of steps (descriptors depend on the
       // step index alone), so the walk is counted once up front.
       int nsteps = 0;
       for (int qt = -1, sub = 0; next_q_step(p, kt, klim, qt, sub);) ++nsteps;
-      for (int j = 0; j < 2 && j < nsteps && ok; ++j) ok = issue_sdp(j);
-      for (int i = 0; ok && i < nsteps; ++i) {
-        const int bf = i & 1;
-        const uint64_t sq_mn = dst_mn + (uint64_t)((i % C::NS) * st_step);
-        const uint64_t ds = dds + (uint64_t)(bf * ds_step);
-        if (!(ok = mbar_wait(bar(C::B_EW + bf), (i >> 1) & 1, ab))) break;
-        tc_fence_after();
-        // dV += P^T dO   (P^T: bf16 in TMEM over S[bf]; dO as MN-major B)
-        mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
-        // dK += dS^T Q
-        mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, i > 0);
-        mma_commit(bar(C::B_EMPTY + i % C::NS));
-        // dQ^T = K^T dS^T over dP[bf]
-        mma_ss_mn_mn_k128(tmem + C::COL_DP + 64 * bf, dk_mn, ds, id_q, 0);
-        mma_commit(bar(C::B_DQF + bf));
-        if (i + 2 < nsteps && !(ok = issue_sdp(i + 2))) break;
+      bool ok = mbar_wait(bar(C::B_KV), 0, ab);
+      tc_fence_after();
+      if (warp == 1) {
+        for (int j = 0; ok && j < nsteps; ++j) {
+          const int bf = j & 1;
+          const uint64_t sq = dst_k + (uint64_t)((j % C::NS) * st_step);
+          if (!(ok = mbar_wait(bar(C::B_FULL + j % C::NS), (j / C::NS) & 1, ab))) break;
+          if (j >= 2 && !(ok = mbar_wait(bar(C::B_SF + bf), ((j - 2) >> 1) & 1, ab))) break;
+          tc_fence_after();
+          if (D == 128)
+            mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
+          else
+            mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
+          if (j >= 2) {
+            if (!(ok = mbar_wait(bar(C::B_DQE + bf), ((j - 2) >> 1) & 1, ab))) break;
+            tc_fence_after();
+          }
+          if (D == 128)
+            mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
+          else
+            mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
+          mma_commit(bar(C::B_S + bf));
+        }
+      } else {
+        for (int i = 0; ok && i < nsteps; ++i) {
+          const int bf = i & 1;
+          const uint64_t sq_mn = dst_mn + (uint64_t)((i % C::NS) * st_step);
+          const uint64_t ds = dds + (uint64_t)(bf * ds_step);
+          if (!(ok = mbar_wait(bar(C::B_EW + bf), (i >> 1) & 1, ab))) break;
+          tc_fence_after();
+          // dV += P^T dO   (P^T: bf16 in TMEM over S[bf]; dO as MN-major B)
+          mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
+          mma_commit(bar(C::B_SF + bf));
+          // dK += dS^T Q
+          mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, i > 0);
+          mma_commit(bar(C::B_EMPTY + i % C::NS));
+          // dQ^T = K^T dS^T over dP[bf]
+          mma_ss_mn_mn_k128(tmem + C::COL_DP + 64 * bf, dk_mn, ds, id_q, 0);
+          mma_commit(bar(C::B_DQF + bf));
+        }
+        // dK and dV are complete once this thread's last MMAs are (the other
+        // issuer's work for the last step finished before it could start)
+        mma_commit(bar(C::B_FIN));
       }
-      mma_commit(bar(C::B_FIN));
-      mma_commit(bar(C::B_DRAIN));
+      mma_commit(bar(C::B_DRAIN + warp - 1));
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(bar(C::B_DRAIN + warp - 1), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
   } else if (warp >= 4 && warp < 8) {

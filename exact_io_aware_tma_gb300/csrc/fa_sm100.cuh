@@ -47,6 +47,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (no suspend window).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Tests two barriers with both probes in flight together.
+__device__ __forceinline__ bool mbar_test2(uint32_t bar0, uint32_t par0, uint32_t bar1,
+                                           uint32_t par1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p, q;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+      " and.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort word of a CTA plus the global status word.
 struct Abort {
   volatile int* flag;  // shared memory
@@ -57,7 +82,7 @@ struct Abort {
 // false (and raises the CTA's abort flag and the global status) on timeout,
 // or false at once if another warp of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
