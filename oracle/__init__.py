@@ -15,3 +15,8 @@ from .attention import (  # noqa: F401
     attention_forward_rows,
     live_tiles,
 )
+from .kvcache import (  # noqa: F401
+    attention_forward_kvcache,
+    kvcache_allowed,
+    merge_partial_states,
+)
