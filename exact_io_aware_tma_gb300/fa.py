@@ -1,4 +1,5 @@
-"""ctypes binding of ``libfa_gb300.so`` (C ABI declared in include/fa.h).
+"""ctypes binding of ``libfa_gb300.so`` (C ABI declared in include/fa.h and
+include/fa_kvcache.h).
 
 Argument marshalling only: every step of attention runs in the library's
 CUDA kernels.  PyTorch provides device memory and the current stream.  If the
@@ -31,7 +32,13 @@ SIGNATURES = {
     "fa_last_device_status": ([_vp], _i),
     "fa_selftest_mma": ([_i, _vp, _vp, _vp, _i, _vp], _i),
     "fa_backward_noalloc": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
+    "fa_kvcache_num_splits": ([_i] * 6, _i),
+    "fa_kvcache_workspace_bytes": ([_i] * 6, _sz),
+    "fa_forward_kvcache": ([_vp] * 5 + [_i] * 5 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
+    "fa_combine": ([_vp, _vp, _i, ctypes.c_longlong, _i, _vp, _vp, _vp], _i),
 }
+
+KVCACHE_MAX_SPLITS = 256  # FA_KVCACHE_MAX_SPLITS (include/fa_kvcache.h)
 
 # Size of the library's built-in backward scratch (include/fa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -161,6 +168,69 @@ def backward_noalloc(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=
     if st != FA_OK:
         raise FAError(st, "fa_backward_noalloc")
     return dq, dk, dv
+
+
+def kvcache_num_splits(B, H, Nq, Nk, d, num_sms=0):
+    """Split count ``forward_kvcache`` picks with ``num_splits=0``."""
+    return int(load().fa_kvcache_num_splits(B, H, Nq, Nk, d, num_sms))
+
+
+def kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits=0):
+    return int(load().fa_kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits))
+
+
+def forward_kvcache(q, k_cache, v_cache, cache_len=None, causal=False, scale=None,
+                    num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """O, LSE of q [B,H,Nq,d] against a [B,H,Nk,d] key/value cache whose
+    first cache_len[b] slots are valid; see include/fa_kvcache.h."""
+    lib = load()
+    for t in (q, k_cache, v_cache):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("q, k_cache, v_cache must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, H, Nk, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must be [B, H, Nk, d] with q's B, H, d")
+    if cache_len is not None and not (cache_len.is_cuda and cache_len.dtype == torch.int32
+                                      and cache_len.is_contiguous()
+                                      and tuple(cache_len.shape) == (B,)):
+        raise ValueError(f"cache_len must be a contiguous int32 CUDA [{B}] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if num_splits == 0:
+        num_splits = kvcache_num_splits(B, H, Nq, Nk, d)
+    nbytes = kvcache_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32) if lse is None else lse
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.fa_forward_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse),
+                                B, H, Nq, Nk, d, scale, int(bool(causal)), _ptr(cache_len),
+                                int(num_splits), _ptr(workspace), wsb, _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_forward_kvcache")
+    return out, lse
+
+
+def combine(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """Merge partial results over disjoint key sets: o_parts fp32 [S, rows, d]
+    (normalised), lse_parts fp32 [S, rows] -> (O bf16 [rows, d], LSE fp32
+    [rows]); see ``fa_combine``."""
+    lib = load()
+    if not (o_parts.is_cuda and o_parts.dtype == torch.float32 and o_parts.is_contiguous()
+            and o_parts.dim() == 3):
+        raise ValueError("o_parts must be a contiguous fp32 CUDA [S, rows, d] tensor")
+    S, rows, d = o_parts.shape
+    if not (lse_parts.is_cuda and lse_parts.dtype == torch.float32
+            and lse_parts.is_contiguous() and tuple(lse_parts.shape) == (S, rows)):
+        raise ValueError(f"lse_parts must be a contiguous fp32 CUDA [{S}, {rows}] tensor")
+    out = torch.empty((rows, d), device=o_parts.device, dtype=torch.bfloat16) if out is None else out
+    lse = torch.empty(rows, device=o_parts.device, dtype=torch.float32) if lse is None else lse
+    st = lib.fa_combine(_ptr(o_parts), _ptr(lse_parts), S, rows, d, _ptr(out), _ptr(lse),
+                        _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_combine")
+    return out, lse
 
 
 def tile_schedule(N, causal=False, block_mask=None, kv_len=None, b=0, device="cuda"):

@@ -39,6 +39,24 @@ WORKLOADS = {
 
 BENCH_WORKLOAD = "long_causal_n8192_d128"
 
+# Attention of new query rows against a key/value cache: name -> shape.  The
+# valid cache length of each batch row is drawn in [len_lo, len_hi]; slots
+# past it hold random values that must not reach the result.
+KVCACHE_WORKLOADS = {
+    "decode_kvcache_b8_h16_nk32768_d128": dict(B=8, H=16, Nq=1, Nk=32768, d=128,
+                                               causal=False, len_lo=16384,
+                                               len_hi=32768, seed=5),
+    "specdecode_kvcache_b8_h16_nq4_nk32768_d128": dict(B=8, H=16, Nq=4, Nk=32768,
+                                                       d=128, causal=True,
+                                                       len_lo=16384, len_hi=32768,
+                                                       seed=6),
+    "decode_kvcache_b32_h12_nk4096_d64": dict(B=32, H=12, Nq=1, Nk=4096, d=64,
+                                              causal=False, len_lo=1024,
+                                              len_hi=4096, seed=7),
+}
+
+KVCACHE_BENCH_WORKLOAD = "decode_kvcache_b8_h16_nk32768_d128"
+
 
 def band_global_block_mask(n_tiles, band=1, global_every=16):
     """uint8 [T, T]: 1 where |i - j| <= band or j % global_every == 0."""
@@ -75,6 +93,31 @@ def make_inputs(B, H, N, d, mask="none", seed=0, kv_lo=None, kv_hi=None,
         raise ValueError(f"unknown mask kind {mask!r}")
     return dict(q=q, k=k, v=v, do=do, causal=causal, block_mask=block_mask,
                 kv_len=kv_len, scale=1.0 / math.sqrt(d))
+
+
+def make_kvcache_inputs(B, H, Nq, Nk, d, causal=False, seed=0, len_lo=None,
+                        len_hi=None):
+    """CPU inputs for attention against a cache.
+
+    ``torch.Generator('cpu').manual_seed(seed)``; Q [B,H,Nq,d], then K and V
+    [B,H,Nk,d], iid N(0, 1) in fp32 rounded to bf16; cache_len (int32 [B])
+    from ``numpy.random.default_rng(seed).integers(len_lo, len_hi + 1)``, or
+    None (every slot valid) when ``len_lo`` is None.
+    """
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    cache_len = None
+    if len_lo is not None:
+        rng = np.random.default_rng(seed)
+        cache_len = rng.integers(len_lo, len_hi + 1, size=B).astype(np.int32)
+    return dict(q=q, k=k, v=v, causal=bool(causal), cache_len=cache_len,
+                scale=1.0 / math.sqrt(d))
+
+
+def kvcache_workload_inputs(name):
+    return make_kvcache_inputs(**KVCACHE_WORKLOADS[name])
 
 
 def workload_inputs(name, with_grad=True):
