@@ -9,6 +9,12 @@ under causal masking, backward 2.5x the forward.
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
 bounded sample of the same workload instead (the baseline arm).
+
+The default line also carries ``kvcache_decode``: attention of one new query
+row per head against a 32768-slot key/value cache (split over the keys, then
+merged), timed on its own and reported in GB/s of K/V streamed against the
+measured HBM bandwidth.  ``--workload decode_kvcache_...`` makes that path
+the line's subject instead.
 """
 
 import argparse
@@ -26,6 +32,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOP/s (bf16) and % of GB300 dense-BF16 tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
 
 
 def peaks():
@@ -196,6 +211,30 @@ def run_reference(args, cfg, name):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_kvcache(args, name):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    vals, secs, desc = [], [], ""
+    for _ in range(max(1, args.steps)):
+        cb = kvcache_oracle_sample(name, 0, budget_s=5.0)
+        vals.append(cb["value"])
+        secs.append(cb["seconds"])
+        desc = cb["sample"]
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": "attention against a KV cache: GB/s of K/V/Q/O moved",
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": len(vals),
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": name},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def traffic_record(kernel):
@@ -353,6 +392,15 @@ def run_gpu(args, cfg, name):
         e2e = {"value": world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
+    kvc = None
+    if not args.no_kvcache:
+        from exact_io_aware_tma_gb300.workloads import KVCACHE_BENCH_WORKLOAD
+        del ws, flush
+        torch.cuda.empty_cache()
+        kvc = time_kvcache(KVCACHE_BENCH_WORKLOAD, args.steps, args.warmup, dev,
+                           rank_seed(0, rank))
+        kvc.pop("inputs")
+
     if rank == 0:
         clocks = clk.summary()
         line = {
@@ -378,23 +426,205 @@ def run_gpu(args, cfg, name):
             "gpu_launches": 4 * args.steps,
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
+            "kvcache_decode": kvc,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- KV cache
+
+def kvcache_bytes(inp):
+    """Algorithmic HBM bytes of one call: the valid K and V slots, Q in, O and
+    LSE out (split partials are an implementation detail and not counted)."""
+    B, H, Nq, d = inp["q"].shape
+    Nk = inp["k"].shape[2]
+    lens = inp["cache_len"]
+    live = B * Nk if lens is None else int(lens.clip(0, Nk).sum())
+    return H * live * d * 2 * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+
+
+def time_kvcache(name, steps, warmup, dev, seed_offset=0):
+    """Event-timed calls of fa_forward_kvcache on a KV-cache workload (inputs
+    resident, far larger than L2, so nothing is flushed).  Returns a dict."""
+    import torch
+    from exact_io_aware_tma_gb300 import fa
+    from exact_io_aware_tma_gb300.workloads import KVCACHE_WORKLOADS, make_kvcache_inputs
+    cfg = dict(KVCACHE_WORKLOADS[name])
+    cfg["seed"] += seed_offset
+    inp = make_kvcache_inputs(**cfg)
+    q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+    cl = None if inp["cache_len"] is None else torch.from_numpy(inp["cache_len"]).to(dev)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    S = fa.kvcache_num_splits(B, H, Nq, Nk, d)
+    wsb = fa.kvcache_workspace_bytes(B, H, Nq, Nk, d, S)
+    ws = torch.empty(max(wsb, 1), device=dev, dtype=torch.uint8)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        fa.forward_kvcache(q, k, v, cache_len=cl, causal=inp["causal"], scale=inp["scale"],
+                           num_splits=S, out=o, lse=lse, workspace=ws, stream=stream)
+
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    status = fa.last_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.status_string(status)}")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = kvcache_bytes(inp)
+    peak, kind = hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": name, "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d,
+            "causal": inp["causal"], "num_splits": S, "us_per_call": 1e3 * ms,
+            "gbs": gbs, "bytes_per_call": nbytes, "hbm_peak_gbs": peak, "peak_kind": kind,
+            "frac_of_hbm": gbs / peak, "launches_per_call": 1 if S == 1 else 2,
+            "inputs": inp}
+
+
+def run_gpu_kvcache(args, name):
+    import torch
+    from exact_io_aware_tma_gb300 import fa
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = kvcache_oracle_sample(name, rank_seed(0, rank))
+    fa.load()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        r = time_kvcache(name, args.steps, args.warmup, dev, rank_seed(0, rank))
+    inp = r.pop("inputs")
+    ms = max_over_ranks(r["us_per_call"] / 1e3, dev)
+    value = world * r["bytes_per_call"] / (ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        e2e = kvcache_e2e(inp, r["num_splits"], args.steps, dev, world)
+    if rank == 0:
+        line = {
+            "metric": "attention against a KV cache: GB/s of K/V/Q/O moved", "value": value,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, **{k: r[k] for k in ("B", "H", "Nq", "Nk", "d",
+                                                               "causal", "num_splits")},
+                       "parallelism": f"replicas{world}",
+                       "l2": "not flushed: inputs (GBs) far exceed the 129 MB L2"},
+            "roofline": {"bound": "hbm", "kernel": "kvcache_split + combine (whole call)",
+                         "achieved": r["gbs"], "peak": r["hbm_peak_gbs"], "unit": "GB/s",
+                         "frac": r["frac_of_hbm"], "peak_kind": r["peak_kind"],
+                         "traffic": None},
+            "cpu_baseline": cpu_base, "e2e": e2e,
+            "gpu_launches": r["launches_per_call"] * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def kvcache_oracle_sample(name, seed_offset=0, budget_s=10.0):
+    """The fp64 oracle on whole heads of a KV-cache workload until budget_s
+    seconds are spent; returns the cpu_baseline dict (GB/s of the same
+    algorithmic bytes)."""
+    from exact_io_aware_tma_gb300.workloads import KVCACHE_WORKLOADS, make_kvcache_inputs, to_f64
+    from oracle import attention_forward_kvcache
+    cfg = dict(KVCACHE_WORKLOADS[name])
+    cfg["seed"] += seed_offset
+    inp = make_kvcache_inputs(**cfg)
+    B, H, Nq, d = inp["q"].shape
+    heads, spent, nbytes = 0, 0.0, 0
+    for b in range(B):
+        for h in range(H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            q, k, v = (to_f64(inp[x][sl]) for x in ("q", "k", "v"))
+            cl = None if inp["cache_len"] is None else inp["cache_len"][b:b + 1]
+            t0 = time.perf_counter()
+            attention_forward_kvcache(q, k, v, inp["scale"], inp["causal"], cl)
+            spent += time.perf_counter() - t0
+            heads += 1
+            L = k.shape[2] if cl is None else int(min(max(cl[0], 0), k.shape[2]))
+            nbytes += L * d * 4 + 2 * Nq * d * 2 + Nq * 4
+            if spent >= budget_s:
+                break
+        if spent >= budget_s:
+            break
+    return {"value": nbytes / spent / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": spent,
+            "sample": f"{heads} whole head(s) of {name} (fp64 numpy, BLAS threads = all cores)"}
+
+
+def kvcache_e2e(inp, S, steps, dev, world):
+    """Same call through the public API with host (pinned) buffers: Q, K, V and
+    cache_len copied in and O, LSE copied out inside the timed region."""
+    import numpy as np
+    import torch
+    from exact_io_aware_tma_gb300 import fa
+    hq, hk, hv = (inp[x].pin_memory() for x in ("q", "k", "v"))
+    lens = inp["cache_len"]
+    hcl = torch.from_numpy(lens if lens is not None else np.zeros(0, np.int32)).pin_memory()
+    q, k, v = (torch.empty_like(x, device=dev) for x in (hq, hk, hv))
+    cl = torch.empty_like(hcl, device=dev)
+    ho = torch.empty_like(hq).pin_memory()
+    B, H, Nq, d = hq.shape
+    hlse = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps + 1)]
+    for a, b in ev:
+        a.record(stream)
+        for h_, d_ in ((hq, q), (hk, k), (hv, v), (hcl, cl)):
+            d_.copy_(h_, non_blocking=True)
+        o, lse = fa.forward_kvcache(q, k, v, cache_len=cl if lens is not None else None,
+                                    causal=inp["causal"],
+                                    scale=inp["scale"], num_splits=S)
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev[1:]), dev)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hcl))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse))
+    return {"value": world * kvcache_bytes(inp) / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
 def main():
-    from exact_io_aware_tma_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
+    from exact_io_aware_tma_gb300.workloads import (BENCH_WORKLOAD, KVCACHE_WORKLOADS,
+                                                    WORKLOADS)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--workload", default=BENCH_WORKLOAD,
+                    choices=list(WORKLOADS) + list(KVCACHE_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kvcache", action="store_true",
+                    help="skip the KV-cache decode figure of the default line")
     args = ap.parse_args()
+    if args.workload in KVCACHE_WORKLOADS:
+        if args.impl == "reference":
+            run_reference_kvcache(args, args.workload)
+        else:
+            run_gpu_kvcache(args, args.workload)
+        return
     cfg = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, cfg, args.workload)

@@ -101,8 +101,9 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
                   float* __restrict__ dq_acc, int npad) {
   using C = BwdTc<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // An offset (not an integer round trip) keeps the pointer visibly in shared
+  // memory, so C++ accesses through it compile to shared-memory instructions.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t s0 = smem_u32(smem);
   const uint32_t bar0 = s0 + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * i; };

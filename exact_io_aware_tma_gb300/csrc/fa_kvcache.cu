@@ -166,8 +166,9 @@ __global__ void __launch_bounds__(THREADS, 2)
                          const __grid_constant__ CUtensorMap tm_v, Params p) {
   using C = Cfg<D, RQ>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Offset (not an integer round trip) keeps the pointer visibly in shared
+  // memory, so the accesses below compile to shared-memory loads and stores.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::OFF_BAR;
   const uint32_t bar_empty = bar_full + C::NS * 8;
@@ -557,9 +558,12 @@ __global__ void __launch_bounds__(THREADS, 2)
 
 // Merge of S partial results per row: o_part [S][rows][d] fp32 (normalised),
 // lse_part [S][rows] (natural log, -inf = empty part) -> o bf16 [rows][d],
-// lse fp32 [rows].  One warp per row, folding the parts in order with the
-// online-normalisation update; every lane carries the running (m, l) of the
-// row and the running u of its columns 4*lane + 128*i.
+// lse fp32 [rows].  One warp per row.  The fold of the parts with the
+// online-normalisation update is evaluated in its closed form, which is the
+// same sum without the serial dependence from part to part: the lanes first
+// find the largest part LSE (M), then every part's weight 2^(LSE_s - M)
+// (lane s % 32 holds part s's weight), and the output loads of all parts are
+// independent of each other.  Empty parts are skipped, their rows unread.
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int S,
                    long long rows, int d, __nv_bfloat16* __restrict__ o,
@@ -569,32 +573,46 @@ __global__ void __launch_bounds__(256)
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int nv = d / 4;  // float4 per row
-  float m = -INFINITY, l = 0.f;
+  float m = -INFINITY;
+  for (int s = lane; s < S; s += 32)
+    m = fmaxf(m, __ldg(lse_part + (long long)s * rows + row) * kLog2e);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   float4 u[MAXV];
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < S; ++s) {
-    const float ms = __ldg(lse_part + (long long)s * rows + row) * kLog2e;
-    if (ms == -INFINITY) continue;  // an empty part adds nothing
-    const float mn = fmaxf(m, ms);
-    const float a_old = fast_exp2(m - mn);  // 0 while nothing was folded (m = -inf)
-    const float a_new = fast_exp2(ms - mn);
-    l = fmaf(a_old, l, a_new);
-    const float4* src = reinterpret_cast<const float4*>(o_part + ((long long)s * rows + row) * d);
+  float lsum = 0.f;
+  if (m != -INFINITY) {
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int s = s0 + lane;
+      // 2^(-inf - M) = 0: an empty part gets weight 0 and is skipped below
+      const float w = s < S ? fast_exp2(__ldg(lse_part + (long long)s * rows + row) * kLog2e - m)
+                            : 0.f;
+      lsum += w;
+      const int n = min(32, S - s0);
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        if (wj == 0.f) continue;  // warp-uniform
+        const float4* src =
+            reinterpret_cast<const float4*>(o_part + ((long long)(s0 + j) * rows + row) * d);
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int c = lane + 32 * i;
-      if (c < nv) {
-        const float4 x = __ldg(src + c);
-        u[i].x = fmaf(a_new, x.x, a_old * u[i].x);
-        u[i].y = fmaf(a_new, x.y, a_old * u[i].y);
-        u[i].z = fmaf(a_new, x.z, a_old * u[i].z);
-        u[i].w = fmaf(a_new, x.w, a_old * u[i].w);
+        for (int i = 0; i < MAXV; ++i) {
+          const int c = lane + 32 * i;
+          if (c < nv) {
+            const float4 x = __ldg(src + c);
+            u[i].x = fmaf(wj, x.x, u[i].x);
+            u[i].y = fmaf(wj, x.y, u[i].y);
+            u[i].z = fmaf(wj, x.z, u[i].z);
+            u[i].w = fmaf(wj, x.w, u[i].w);
+          }
+        }
       }
     }
-    m = mn;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int c = lane + 32 * i;
@@ -604,7 +622,7 @@ __global__ void __launch_bounds__(256)
       *reinterpret_cast<uint2*>(o + row * d + 4 * c) = w;
     }
   }
-  if (lane == 0) lse[row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  if (lane == 0) lse[row] = lsum > 0.f ? (m + log2f(lsum)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host

@@ -21,8 +21,9 @@ __global__ void __launch_bounds__(128, 1)
                     const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16* a_glob,
                     float* c, int mode, int n, int* status) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // An offset (not an integer round trip) keeps the pointer visibly in shared
+  // memory, so C++ accesses through it compile to shared-memory instructions.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + 2 * kHalf;
   const uint32_t bars = sB + 2 * kHalf;  // [0] tma, [1] mma

@@ -23,8 +23,9 @@
  * run on different CTAs; each yields a normalised partial output O_s and
  * its LSE_s, and the parts are folded with the running-max / running-sum /
  * rescaled-accumulator update, treating (O_s, LSE_s) as the state
- * m = LSE_s, l = 1, u = O_s.  The result equals the unsplit one up to
- * floating-point rounding.
+ * m = LSE_s, l = 1, u = O_s (the kernel evaluates the fold in its closed
+ * form LSE = log sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s).  The
+ * result equals the unsplit one up to floating-point rounding.
  *
  * Layouts (row-major, device memory, caller-owned):
  *   q, o              : bf16 [B, H, Nq, d], 16-byte aligned
