@@ -13,6 +13,8 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_forward_online,
     attention_forward_rows,
+    attention_backward_varlen,
+    attention_forward_varlen,
     live_tiles,
 )
 from .kvcache import (  # noqa: F401

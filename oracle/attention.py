@@ -38,11 +38,24 @@ What it computes, and where the pages define it:
   is allowed only if its tile is nonzero (page "Fast and Memory Efficient
   Exact Attention", "Summary & Methodology Analysis": zero blocks of a
   predefined block-sparsity mask are skipped).
+* Sliding-window masks and variable-length sequences (page "FlashAttention",
+  aiwiki, section "Software integration and limitations": the method's
+  software offers causal and sliding-window masks and variable-length
+  sequences).  The pages give no formula for either; the readings below are
+  the plain ones.
 
 Readings where the pages are silent (each is listed in the design notes):
 * allowed(b, i, j) = (not causal or j <= i)
                      and (block_mask is None or block_mask[i//128][j//128] != 0)
-                     and (kv_len is None or j < kv_len[b]).
+                     and (kv_len is None or j < kv_len[b])
+                     and (window_left is None or j >= i - window_left)
+                     and (window_right is None or j <= i + window_right).
+  A window of (w, 0) with causal is the usual causal sliding window: query i
+  sees keys i-w .. i.
+* Variable-length sequences come packed: Q, K, V of shape [T, H, d] hold the
+  B sequences back to back, sequence b being rows cu_seqlens[b] ..
+  cu_seqlens[b+1]-1; each sequence attends only within itself, as a batch
+  element of length cu_seqlens[b+1] - cu_seqlens[b] would.
 * A row with no allowed key has O_i = 0, LSE_i = -inf and contributes no
   gradient.
 * Inputs are whatever arrays the caller passes (the tests pass the bf16
@@ -55,16 +68,23 @@ TILE = 128  # side of one block-mask tile, in queries and in keys
 
 
 def allowed_mask(n, rows=None, causal=False, block_mask=None, kv_len=None,
-                 tile=TILE):
+                 tile=TILE, window=None):
     """Boolean [len(rows), n]: which (query row, key column) pairs may interact.
 
-    ``kv_len`` is the scalar valid-key count of ONE batch element (or None).
+    ``kv_len`` is the scalar valid-key count of ONE batch element (or None);
+    ``window`` = (left, right), either bound None (or negative) = unbounded.
     """
     rows = np.arange(n) if rows is None else np.asarray(rows)
     cols = np.arange(n)
     ok = np.ones((rows.shape[0], n), dtype=bool)
     if causal:
         ok &= cols[None, :] <= rows[:, None]
+    if window is not None:
+        left, right = window
+        if left is not None and left >= 0:
+            ok &= cols[None, :] >= rows[:, None] - left
+        if right is not None and right >= 0:
+            ok &= cols[None, :] <= rows[:, None] + right
     if block_mask is not None:
         bm = np.asarray(block_mask)
         ok &= bm[rows[:, None] // tile, cols[None, :] // tile] != 0
@@ -96,7 +116,8 @@ def _kv(kv_len, b):
 
 
 def attention_forward(q, k, v, scale, causal=False, block_mask=None,
-                      kv_len=None, heads=None, row_chunk=1024, tile=TILE):
+                      kv_len=None, heads=None, row_chunk=1024, tile=TILE,
+                      window=None):
     """O [B,H,N,dv] and LSE [B,H,N] by the textbook two-pass definition.
 
     ``heads`` optionally restricts the work to a list of (b, h) pairs; the
@@ -112,26 +133,27 @@ def attention_forward(q, k, v, scale, causal=False, block_mask=None,
             rows = np.arange(r0, min(N, r0 + row_chunk))
             s = scale * (q[b, h, rows] @ k[b, h].T)
             ok = allowed_mask(N, rows, causal, block_mask, _kv(kv_len, b),
-                              tile)
+                              tile, window)
             p, lse[b, h, rows] = _softmax_rows(s, ok)
             o[b, h, rows] = p @ v[b, h]
     return o, lse
 
 
 def attention_forward_rows(q, k, v, scale, b, h, rows, causal=False,
-                           block_mask=None, kv_len=None, tile=TILE):
+                           block_mask=None, kv_len=None, tile=TILE, window=None):
     """O and LSE of selected query rows of one head (sampled full-size checks)."""
     q, k, v = _as64(q[b, h]), _as64(k[b, h]), _as64(v[b, h])
     rows = np.asarray(rows)
     s = scale * (q[rows] @ k.T)
     ok = allowed_mask(k.shape[0], rows, causal, block_mask, _kv(kv_len, b),
-                      tile)
+                      tile, window)
     p, lse = _softmax_rows(s, ok)
     return p @ v, lse
 
 
 def attention_backward(q, k, v, do, scale, causal=False, block_mask=None,
-                       kv_len=None, heads=None, row_chunk=1024, tile=TILE):
+                       kv_len=None, heads=None, row_chunk=1024, tile=TILE,
+                       window=None):
     """dQ, dK, dV [B,H,N,d] of L = sum(O * dO), plus O, LSE and D.
 
     P is rebuilt here from the inputs (the oracle stores nothing between
@@ -154,7 +176,7 @@ def attention_backward(q, k, v, do, scale, causal=False, block_mask=None,
             rows = np.arange(r0, min(N, r0 + row_chunk))
             s = scale * (q[b, h, rows] @ k[b, h].T)
             ok = allowed_mask(N, rows, causal, block_mask, _kv(kv_len, b),
-                              tile)
+                              tile, window)
             p, lse[b, h, rows] = _softmax_rows(s, ok)
             o_r = p @ v[b, h]
             o[b, h, rows] = o_r
@@ -169,7 +191,8 @@ def attention_backward(q, k, v, do, scale, causal=False, block_mask=None,
 
 
 def attention_forward_online(q, k, v, scale, causal=False, block_mask=None,
-                             kv_len=None, block_q=128, block_k=128, tile=TILE):
+                             kv_len=None, block_q=128, block_k=128, tile=TILE,
+                             window=None):
     """O and LSE by the tiled online-softmax recurrence (self-check path).
 
     Visits query blocks of ``block_q`` rows and, for each, key blocks of
@@ -191,7 +214,7 @@ def attention_forward_online(q, k, v, scale, causal=False, block_mask=None,
                     cols = np.arange(c0, min(N, c0 + block_k))
                     s_b = scale * (q[b, h, rows] @ k[b, h, cols].T)
                     ok = allowed_mask(N, rows, causal, block_mask,
-                                      _kv(kv_len, b), tile)[:, cols]
+                                      _kv(kv_len, b), tile, window)[:, cols]
                     s_b = np.where(ok, s_b, -np.inf)
                     m_new = np.maximum(m, s_b.max(axis=1))
                     # e^{m - m'}: 0 when nothing was seen yet (m = -inf);
@@ -212,7 +235,8 @@ def attention_forward_online(q, k, v, scale, causal=False, block_mask=None,
     return o, lse
 
 
-def live_tiles(n, causal=False, block_mask=None, kv_len=None, tile=TILE):
+def live_tiles(n, causal=False, block_mask=None, kv_len=None, tile=TILE,
+               window=None):
     """Live (query tile, key tile) pairs of one batch element, by brute force.
 
     A tile pair is live when at least one of its (i, j) pairs is allowed; it
@@ -221,7 +245,7 @@ def live_tiles(n, causal=False, block_mask=None, kv_len=None, tile=TILE):
     tiled kernels must visit (tiles with no allowed pair are skipped).
     """
     t = (n + tile - 1) // tile
-    ok = allowed_mask(n, None, causal, block_mask, kv_len, tile)
+    ok = allowed_mask(n, None, causal, block_mask, kv_len, tile, window)
     out = {}
     for qt in range(t):
         r = slice(qt * tile, min(n, (qt + 1) * tile))
@@ -231,3 +255,51 @@ def live_tiles(n, causal=False, block_mask=None, kv_len=None, tile=TILE):
             if blk.any():
                 out[(qt, kt)] = int(not blk.all())
     return out
+
+
+def _varlen_heads(x, cu_seqlens, b):
+    """Rows of sequence b of a packed [T, H, d] array, as a [1, H, len, d] view."""
+    lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+    return np.transpose(_as64(x)[lo:hi], (1, 0, 2))[None]
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens, scale, causal=False,
+                             window=None):
+    """O [T,H,d] and LSE [H,T] of packed variable-length sequences: every
+    sequence b (rows cu_seqlens[b] .. cu_seqlens[b+1]-1) attends within
+    itself by the same definition as a batch element of its own length."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    T, H, _ = q.shape
+    o = np.zeros(v.shape)
+    lse = np.full((H, T), -np.inf)
+    for b in range(len(cu_seqlens) - 1):
+        lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        if hi <= lo:
+            continue
+        ob, lb = attention_forward(_varlen_heads(q, cu_seqlens, b),
+                                   _varlen_heads(k, cu_seqlens, b),
+                                   _varlen_heads(v, cu_seqlens, b), scale,
+                                   causal=causal, window=window)
+        o[lo:hi] = np.transpose(ob[0], (1, 0, 2))
+        lse[:, lo:hi] = lb[0]
+    return o, lse
+
+
+def attention_backward_varlen(q, k, v, do, cu_seqlens, scale, causal=False,
+                              window=None):
+    """dQ, dK, dV [T,H,d], O [T,H,d] and LSE [H,T] of packed sequences, each
+    sequence's gradient being that of its own attention."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    T, H, _ = q.shape
+    dq, dk, dv, o = (np.zeros(x.shape) for x in (q, k, v, v))
+    lse = np.full((H, T), -np.inf)
+    for b in range(len(cu_seqlens) - 1):
+        lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        if hi <= lo:
+            continue
+        r = attention_backward(*(_varlen_heads(x, cu_seqlens, b) for x in (q, k, v, do)),
+                               scale, causal=causal, window=window)
+        for dst, src in zip((dq, dk, dv, o), r[:4]):
+            dst[lo:hi] = np.transpose(src[0], (1, 0, 2))
+        lse[:, lo:hi] = r[4][0]
+    return dq, dk, dv, o, lse
