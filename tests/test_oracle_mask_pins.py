@@ -30,8 +30,8 @@ def test_zero_window_is_the_diagonal():
     # window (0, 0): row i sees key i only -> O_i = V_i, LSE_i = scale q_i.k_i
     q, k, v = rand(2, 2, 9, 5), rand(2, 2, 9, 5), rand(2, 2, 9, 5)
     o, lse = attention_forward(q, k, v, 0.3, window=(0, 0))
-    np.testing.assert_allclose(o, v, atol=1e-15)
-    np.testing.assert_allclose(lse, 0.3 * np.sum(q * k, axis=-1), atol=1e-14)
+    np.testing.assert_allclose(o, v, atol=1e-15, rtol=0)
+    np.testing.assert_allclose(lse, 0.3 * np.sum(q * k, axis=-1), atol=1e-14, rtol=0)
 
 
 def test_causal_window_of_one_is_two_key_softmax():
@@ -39,13 +39,13 @@ def test_causal_window_of_one_is_two_key_softmax():
     n, d = 7, 3
     q, k, v = rand(1, 1, n, d), rand(1, 1, n, d), rand(1, 1, n, d)
     o, _ = attention_forward(q, k, v, 1.0, causal=True, window=(1, -1))
-    np.testing.assert_allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-15)
+    np.testing.assert_allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-15, rtol=0)
     for i in range(1, n):
         a = q[0, 0, i] @ k[0, 0, i - 1]
         b = q[0, 0, i] @ k[0, 0, i]
         w = 1.0 / (1.0 + math.exp(b - a))  # weight of key i-1
         np.testing.assert_allclose(o[0, 0, i], w * v[0, 0, i - 1] + (1 - w) * v[0, 0, i],
-                                   atol=1e-14)
+                                   atol=1e-14, rtol=0)
 
 
 def test_wide_window_is_no_window():
@@ -108,15 +108,15 @@ def test_window_against_sdpa_and_autograd(window, causal):
     q, k, v, do = (rand(1, 2, n, d) for _ in range(4))
     ok = _window_ok(n, causal, *window)
     o, lse = attention_forward(q, k, v, 0.45, causal=causal, window=window)
-    np.testing.assert_allclose(o[0], _sdpa(q[0], k[0], v[0], 0.45, ok), atol=1e-13)
+    np.testing.assert_allclose(o[0], _sdpa(q[0], k[0], v[0], 0.45, ok), atol=1e-13, rtol=0)
     np.testing.assert_array_equal(allowed_mask(n, None, causal, window=window), ok)
     dq, dk, dv = attention_backward(q, k, v, do, 0.45, causal=causal, window=window)[:3]
     qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
     s = (0.45 * qt @ kt.transpose(-1, -2)).masked_fill(~torch.tensor(ok), -math.inf)
     (torch.softmax(s, -1) @ vt * torch.tensor(do)).sum().backward()
-    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12)
-    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12)
-    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12, rtol=0)
 
 
 def _packed(lens, H, d):
@@ -143,16 +143,16 @@ def test_varlen_against_block_diagonal_sdpa(causal, window):
     o, lse = attention_forward_varlen(q, k, v, cu, 0.5, causal, window)
     qh, kh, vh = (np.transpose(x, (1, 0, 2)) for x in (q, k, v))
     ref = _sdpa(qh, kh, vh, 0.5, ok)
-    np.testing.assert_allclose(np.transpose(o, (1, 0, 2)), ref, atol=1e-13)
+    np.testing.assert_allclose(np.transpose(o, (1, 0, 2)), ref, atol=1e-13, rtol=0)
     s = torch.tensor(0.5 * qh @ np.swapaxes(kh, -1, -2)).masked_fill(~torch.tensor(ok), -math.inf)
-    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), atol=1e-13)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), atol=1e-13, rtol=0)
     # gradients through torch autograd over the packed sequence
     dq, dk, dv = attention_backward_varlen(q, k, v, do, cu, 0.5, causal, window)[:3]
     qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (qh, kh, vh))
     sc = (0.5 * qt @ kt.transpose(-1, -2)).masked_fill(~torch.tensor(ok), -math.inf)
     (torch.softmax(sc, -1) @ vt * torch.tensor(np.transpose(do, (1, 0, 2)))).sum().backward()
     for got, t in ((dq, qt), (dk, kt), (dv, vt)):
-        np.testing.assert_allclose(np.transpose(got, (1, 0, 2)), t.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(np.transpose(got, (1, 0, 2)), t.grad.numpy(), atol=1e-12, rtol=0)
 
 
 # -------------------------------------------------- (d) finite differences
