@@ -139,9 +139,13 @@ static bool aligned(const void* ptr, size_t a) {
   return (reinterpret_cast<uintptr_t>(ptr) % a) == 0;
 }
 
-// Shared size checks.  Fills `p` on success.
-static int check_sizes(int B, int H, int N, int d, float scale, int causal,
-                       const uint8_t* block_mask, const int32_t* kv_len, Problem* p) {
+// Shared size checks.  Fills `p` on success.  Window sides of N or more
+// allow every key on that side and are stored as unbounded (-1), which also
+// keeps i + wr within int range.  A scale whose scale*log2(e) is zero or
+// subnormal is held at +-1e-30 in log2 units: the scores it produces are
+// still 0 to within fp32 rounding (uniform attention), while a masked score
+// (+-inf) still maps to -inf, where 0 * inf would give NaN.
+static int check_sizes(int B, int H, int N, int d, float scale, const fa_mask* m, Problem* p) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -157,12 +161,26 @@ static int check_sizes(int B, int H, int N, int d, float scale, int causal,
   p->d = d;
   p->T = (int)T;
   p->scale = scale;
-  p->scale_log2 = scale * kLog2e;
-  p->causal = causal ? 1 : 0;
-  p->block_mask = block_mask;
-  p->kv_len = kv_len;
+  float sl = scale * kLog2e;
+  if (std::fabs(sl) < 1e-30f) sl = sl < 0.f ? -1e-30f : 1e-30f;
+  p->scale_log2 = sl;
+  p->causal = (m != nullptr && m->causal) ? 1 : 0;
+  p->wl = (m != nullptr && m->window_left >= 0 && m->window_left < N) ? m->window_left : -1;
+  p->wr = (m != nullptr && m->window_right >= 0 && m->window_right < N) ? m->window_right : -1;
+  p->block_mask = m != nullptr ? m->block_mask : nullptr;
+  p->kv_len = m != nullptr ? m->kv_len : nullptr;
   p->status = nullptr;
   return FA_OK;
+}
+
+static fa_mask plain_mask(int causal, const uint8_t* block_mask, const int32_t* kv_len) {
+  fa_mask m;
+  m.causal = causal;
+  m.window_left = -1;
+  m.window_right = -1;
+  m.block_mask = block_mask;
+  m.kv_len = kv_len;
+  return m;
 }
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -185,15 +203,14 @@ const char* fa_status_string(int s) {
   }
 }
 
-int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-               int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
-               const int32_t* kv_len, void* stream) {
+int fa_forward_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int N, int d, float scale, const fa_mask* mask, void* stream) {
   Problem p;
-  int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
+  int st = check_sizes(B, H, N, d, scale, mask, &p);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(lse, 4) || !aligned(kv_len, 4))
+      !aligned(lse, 4) || !aligned(p.kv_len, 4))
     return FA_ERR_INVALID_ARG;
   p.status = status_word();
   if (p.status == nullptr) return FA_ERR_CUDA;
@@ -201,9 +218,16 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+               int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+               const int32_t* kv_len, void* stream) {
+  const fa_mask m = plain_mask(causal, block_mask, kv_len);
+  return fa_forward_masked(q, k, v, o, lse, B, H, N, d, scale, &m, stream);
+}
+
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   Problem p;
-  if (check_sizes(B, H, N, d, 1.0f, 0, nullptr, nullptr, &p) != FA_OK) return 0;
+  if (check_sizes(B, H, N, d, 1.0f, nullptr, &p) != FA_OK) return 0;
   const size_t vec = round_up((size_t)B * H * padded_rows(N) * sizeof(float), 256);
   return 2 * vec + round_up((size_t)B * H * N * d * sizeof(float), 256);
 }
@@ -237,7 +261,7 @@ static unsigned elementwise_blocks(long long chunks) {
 int fa_backward_preprocess(const void* o, const void* dout, const float* lse, int B, int H,
                            int N, int d, void* workspace, size_t workspace_bytes, void* stream) {
   Problem p;
-  int st = check_sizes(B, H, N, d, 1.0f, 0, nullptr, nullptr, &p);
+  int st = check_sizes(B, H, N, d, 1.0f, nullptr, &p);
   if (st != FA_OK) return st;
   if (!o || !dout || !lse || !aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
@@ -260,17 +284,15 @@ int fa_backward_preprocess(const void* o, const void* dout, const float* lse, in
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
-                     void* dv, int B, int H, int N, int d,
-                     float scale, int causal, const uint8_t* block_mask,
-                     const int32_t* kv_len, void* workspace, size_t workspace_bytes,
-                     void* stream) {
+static int backward_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                         void* dv, int B, int H, int N, int d, float scale, const fa_mask* mask,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   Problem p;
-  int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
+  int st = check_sizes(B, H, N, d, scale, mask, &p);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) ||
-      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(kv_len, 4))
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(p.kv_len, 4))
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
@@ -283,10 +305,19 @@ int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* do
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                     void* dv, int B, int H, int N, int d, float scale, int causal,
+                     const uint8_t* block_mask, const int32_t* kv_len, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  const fa_mask m = plain_mask(causal, block_mask, kv_len);
+  return backward_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, &m, workspace, workspace_bytes,
+                       stream);
+}
+
 int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
                            const void* workspace, size_t workspace_bytes, void* stream) {
   Problem p;
-  int st = check_sizes(B, H, N, d, scale, 0, nullptr, nullptr, &p);
+  int st = check_sizes(B, H, N, d, scale, nullptr, &p);
   if (st != FA_OK) return st;
   if (!dq || !aligned(dq, 16)) return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
@@ -299,43 +330,58 @@ int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_backward(const void* q, const void* k, const void* v, const void* o,
-                const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
-                const int32_t* kv_len, void* workspace, size_t workspace_bytes,
-                void* stream) {
+int fa_backward_masked(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, float scale, const fa_mask* mask, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   Problem p;
-  int st = check_sizes(B, H, N, d, scale, causal, block_mask, kv_len, &p);
+  int st = check_sizes(B, H, N, d, scale, mask, &p);
   if (st != FA_OK) return st;
   // Validate every argument before the first launch, so a rejected call
   // writes nothing.
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
-      !aligned(lse, 4) || !aligned(kv_len, 4))
+      !aligned(lse, 4) || !aligned(p.kv_len, 4))
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   st = fa_backward_preprocess(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream);
   if (st != FA_OK) return st;
-  st = fa_backward_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, causal, block_mask, kv_len,
-                        workspace, workspace_bytes, stream);
+  st = backward_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, mask, workspace, workspace_bytes,
+                     stream);
   if (st != FA_OK) return st;
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o,
+                const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
+                const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  const fa_mask m = plain_mask(causal, block_mask, kv_len);
+  return fa_backward_masked(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, &m, workspace,
+                            workspace_bytes, stream);
+}
+
+int fa_tile_schedule_masked(int N, const fa_mask* mask, int b, int32_t* row_ptr,
+                            int32_t* col_idx, uint8_t* partial, void* stream) {
+  Problem p;
+  int st = check_sizes(1, 1, N, 64, 1.0f, mask, &p);
+  if (st != FA_OK) return st;
+  if (!row_ptr || !col_idx || !partial || b < 0) return FA_ERR_INVALID_ARG;
+  if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(p.kv_len, 4))
+    return FA_ERR_INVALID_ARG;
+  tile_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(p, b, row_ptr,
+                                                                          col_idx, partial);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_tile_schedule(int N, int causal, const uint8_t* block_mask, const int32_t* kv_len,
                      int b, int32_t* row_ptr, int32_t* col_idx, uint8_t* partial,
                      void* stream) {
-  Problem p;
-  int st = check_sizes(1, 1, N, 64, 1.0f, causal, block_mask, kv_len, &p);
-  if (st != FA_OK) return st;
-  if (!row_ptr || !col_idx || !partial || b < 0) return FA_ERR_INVALID_ARG;
-  if (!aligned(row_ptr, 4) || !aligned(col_idx, 4) || !aligned(kv_len, 4))
-    return FA_ERR_INVALID_ARG;
-  tile_schedule_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(p, b, row_ptr,
-                                                                          col_idx, partial);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const fa_mask m = plain_mask(causal, block_mask, kv_len);
+  return fa_tile_schedule_masked(N, &m, b, row_ptr, col_idx, partial, stream);
 }
 
 int fa_last_device_status(void* stream) {

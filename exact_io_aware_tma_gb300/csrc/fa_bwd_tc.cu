@@ -72,9 +72,10 @@ struct BwdTc {
 };
 
 // Next 64-row query step after (qt, sub) for key tile kt: live query tiles
-// in ascending order, two halves each, skipping halves past N.  Without a
-// block mask the live query tiles are contiguous (causal: from kt on), so the
-// first one is found in closed form.
+// in ascending order within the key tile's query-tile range (exact without a
+// block mask; recomputed here from the constant parameters rather than kept
+// live in registers across the roles' loops), two halves each, skipping
+// halves past N.
 __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, int& qt,
                                             int& sub) {
   if (qt >= 0 && sub == 0 && qt * 128 + 64 < p.N) {
@@ -82,12 +83,11 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, 
     return true;
   }
   sub = 0;
-  if (p.block_mask == nullptr) {
-    if (kt * kTile >= klim) return false;  // dead key tile
-    qt = qt < 0 ? (p.causal ? kt : 0) : qt + 1;
-    return qt < p.T;
-  }
-  for (++qt; qt < p.T; ++qt)
+  int qf, ql;
+  ktile_query_tiles(p, kt, klim, qf, ql);
+  qt = qt < 0 ? qf : qt + 1;
+  if (p.block_mask == nullptr) return qt <= ql;
+  for (; qt <= ql; ++qt)
     if (tile_live(p, qt, kt, klim)) return true;
   return false;
 }
@@ -275,10 +275,23 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       uint32_t sr[64], pr[64];
       tmem_ld64(lane_base + C::COL_S + 64 * bf, sr);
       tmem_ld64(lane_base + C::COL_DP + 64 * bf, pr);
-      // queries c allowed for this key: c >= lo (causal) and key < klim
-      int lo = 0;
-      if (j >= klim) lo = 64;
-      else if (p.causal && j > q0) lo = j - q0;
+      // queries c of the step allowed for this key: lo <= c < hi.  Only
+      // whether the step has disallowed queries is kept through the loop;
+      // they are zeroed in the packed words afterwards.
+      auto q_range = [&](int& lo, int& hi) {
+        lo = 64;
+        hi = 64;
+        if (j < klim) {
+          lo = max(0, col_q_lo(p, j) - q0);
+          hi = min(64, col_q_hi(p, j) + 1 - q0);
+        }
+      };
+      bool edge;
+      {
+        int lo, hi;
+        q_range(lo, hi);
+        edge = lo > 0 || hi < 64;
+      }
       uint32_t pk[32], dk[32];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
@@ -289,14 +302,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
              -L.y);
         fma2(x2, x3, __uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3]), cl2, cl2,
              -L.z, -L.w);
-        float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2), p3 = fast_exp2(x3);
-        if (lo > 0) {
-          const int c = 4 * c4;
-          if (c < lo) p0 = 0.f;
-          if (c + 1 < lo) p1 = 0.f;
-          if (c + 2 < lo) p2 = 0.f;
-          if (c + 3 < lo) p3 = 0.f;
-        }
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2),
+                    p3 = fast_exp2(x3);
         float e0, e1, e2, e3;
         add2(e0, e1, __uint_as_float(pr[4 * c4]), __uint_as_float(pr[4 * c4 + 1]), -Dd.x, -Dd.y);
         add2(e2, e3, __uint_as_float(pr[4 * c4 + 2]), __uint_as_float(pr[4 * c4 + 3]), -Dd.z, -Dd.w);
@@ -304,6 +311,19 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
         pk[2 * c4 + 1] = pack_bf16(p2, p3);
         dk[2 * c4] = pack_bf16(p0 * e0, p1 * e1);
         dk[2 * c4 + 1] = pack_bf16(p2 * e2, p3 * e3);
+      }
+      if (edge) {
+        // disallowed queries: P and dS are 0 (the values computed for them
+        // above, possibly non-finite, are discarded half-word by half-word)
+        int lo, hi;
+        q_range(lo, hi);
+#pragma unroll
+        for (int w = 0; w < 32; ++w) {
+          const uint32_t keep = ((2 * w >= lo && 2 * w < hi) ? 0x0000ffffu : 0u) |
+                                ((2 * w + 1 >= lo && 2 * w + 1 < hi) ? 0xffff0000u : 0u);
+          pk[w] &= keep;
+          dk[w] &= keep;
+        }
       }
       tmem_st32(lane_base + C::COL_S + 64 * bf, pk);
       // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of

@@ -1,5 +1,5 @@
 // Shared device helpers of the attention kernels: the allowed-pair predicate,
-// the live-tile walk, bf16 packing and the warp-level tensor-core fragments.
+// the live-tile walk, bf16 packing and the exp2 used by every softmax.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -19,6 +19,8 @@ struct Problem {
   float scale;            // multiplies Q K^T
   float scale_log2;       // scale * log2(e): scores are kept in log2 units
   int causal;
+  int wl, wr;             // sliding window: j >= i - wl (wl >= 0), j <= i + wr
+                          // (wr >= 0); -1 = unbounded on that side
   const uint8_t* block_mask;  // [T, T] or nullptr
   const int32_t* kv_len;      // [B] or nullptr
   int* status;                // device error word (bounded waits record here)
@@ -31,25 +33,89 @@ __device__ __forceinline__ int key_limit(const Problem& p, int b) {
   return l < 0 ? 0 : (l > p.N ? p.N : l);
 }
 
-// A (query tile, key tile) pair is live when some (i, j) in it is allowed.
-// With equal query and key lengths the causal rule keeps kt <= qt.
-__device__ __forceinline__ bool tile_live(const Problem& p, int qt, int kt,
-                                          int klim) {
+// The keys query row i may attend form one interval [row_key_lo, row_key_hi]
+// (empty when lo > hi), and the queries key column j (< klim) serves form
+// [col_q_lo, col_q_hi]; all four ends are nondecreasing in the row/column.
+__device__ __forceinline__ int row_key_lo(const Problem& p, int i) {
+  return p.wl >= 0 ? max(0, i - p.wl) : 0;
+}
+__device__ __forceinline__ int row_key_hi(const Problem& p, int i, int klim) {
+  int h = klim - 1;
+  if (p.causal) h = min(h, i);
+  if (p.wr >= 0) h = min(h, i + p.wr);
+  return h;
+}
+__device__ __forceinline__ int col_q_lo(const Problem& p, int j) {
+  int l = p.causal ? j : 0;
+  if (p.wr >= 0) l = max(l, j - p.wr);
+  return l;
+}
+__device__ __forceinline__ int col_q_hi(const Problem& p, int j) {
+  return p.wl >= 0 ? min(p.N - 1, j + p.wl) : p.N - 1;
+}
+
+// A (query tile, key tile) pair is live when some allowed (i, j) lies in it:
+// some row i of the tile has keys in the tile's key range.  By the
+// monotonicity above that is: the rows i with row_key_lo(i) <= jmax (i.e.
+// i <= jmax + wl) and row_key_hi(i) >= jmin (i.e. i >= col_q_lo(jmin), given
+// jmin < klim) include one of the tile.  With equal query and key lengths
+// the causal rule alone keeps kt <= qt.
+__device__ __forceinline__ bool tile_live(const Problem& p, int qt, int kt, int klim) {
+  const int jmin = kt * kTile;
+  if (jmin >= klim) return false;
   if (p.causal && kt > qt) return false;
-  if (kt * kTile >= klim) return false;
+  if (p.wl >= 0 || p.wr >= 0) {
+    const int imin = qt * kTile, imax = min(p.N, imin + kTile) - 1;
+    const int jmax = min(klim, jmin + kTile) - 1;
+    const int ilo = max(imin, col_q_lo(p, jmin));
+    const int ihi = p.wl >= 0 ? min(imax, jmax + p.wl) : imax;
+    if (ilo > ihi) return false;
+  }
   if (p.block_mask != nullptr && __ldg(p.block_mask + (size_t)qt * p.T + kt) == 0)
     return false;
   return true;
 }
 
 // A live tile needs element masking when some in-range (i, j) of it is not
-// allowed: the causal diagonal tile, or a tile crossing the key limit.
-__device__ __forceinline__ bool tile_partial(const Problem& p, int qt, int kt,
-                                             int klim) {
-  // Causal diagonal tile: some j > i exists once it holds two rows in range.
-  if (p.causal && kt == qt && p.N - qt * kTile > 1) return true;
-  // Key limit inside the tile's in-range columns.
-  return klim < min(p.N, (kt + 1) * kTile);
+// allowed: its last row's interval starts after the first key, or its first
+// row's interval ends before the last in-range key (the causal diagonal tile,
+// a tile crossing the key limit, the edges of a window).
+__device__ __forceinline__ bool tile_partial(const Problem& p, int qt, int kt, int klim) {
+  const int imin = qt * kTile, imax = min(p.N, imin + kTile) - 1;
+  const int jmin = kt * kTile, jn = min(p.N, jmin + kTile) - 1;
+  if (row_key_lo(p, imax) > jmin) return true;
+  return row_key_hi(p, imin, klim) < jn;
+}
+
+// Without a block mask the live key tiles of query tile qt are exactly
+// [first, last] (first > last: none): rows with no key are only ever the
+// last rows of a tile, so the union of the rows' intervals runs from the
+// first row's start to the last row's end.
+__device__ __forceinline__ void qtile_key_tiles(const Problem& p, int qt, int klim, int& first,
+                                                int& last) {
+  const int imin = qt * kTile, imax = min(p.N, imin + kTile) - 1;
+  const int lo = row_key_lo(p, imin), hi = row_key_hi(p, imax, klim);
+  if (lo > hi) {
+    first = 0;
+    last = -1;
+  } else {
+    first = lo / kTile;
+    last = hi / kTile;
+  }
+}
+
+// Likewise the live query tiles of key tile kt without a block mask.
+__device__ __forceinline__ void ktile_query_tiles(const Problem& p, int kt, int klim, int& first,
+                                                  int& last) {
+  const int jmin = kt * kTile;
+  if (jmin >= klim) {
+    first = 0;
+    last = -1;
+    return;
+  }
+  const int jmax = min(klim, jmin + kTile) - 1;
+  first = col_q_lo(p, jmin) / kTile;
+  last = col_q_hi(p, jmax) / kTile;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -59,53 +125,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// ---- Ampere-style async copy, ldmatrix and mma.sync (warp-level path) ----
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool valid) {
-  int n = valid ? 16 : 0;  // zero-fill when the source row is out of range
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
-               "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::);
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                        uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
-__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Byte offset of 16-byte chunk `c` of row `r` in a row-major bf16 tile whose
-// rows hold `chunks` chunks (a power of two), with the chunk index XOR-
-// swizzled by the row so that eight rows read at one column hit different
-// bank groups.
-__device__ __forceinline__ uint32_t swz(int r, int c, int chunks) {
-  int m = chunks >= 8 ? 7 : chunks - 1;
-  return (uint32_t)((r * chunks + (c ^ (r & m))) * 16);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

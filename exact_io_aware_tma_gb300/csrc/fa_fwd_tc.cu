@@ -58,20 +58,14 @@ struct FwdTc {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-// Last key tile of the union of live tiles of query tiles q0 and q1 (q1 < 0:
-// absent) when there is no block mask: the live tiles are then exactly
-// 0..last (key limit, and the causal rule kt <= qt).
-__device__ __forceinline__ int union_last(const Problem& p, int q0, int q1, int klim) {
-  int last = klim > 0 ? (klim - 1) / kTile : -1;
-  if (p.causal) last = min(last, max(q0, q1));
-  return last;
-}
-
-// Next key tile after kt that is live for query tile q0 or q1.
+// Next key tile after kt that is live for query tile q0 or q1, within the
+// union's range [first, last] (the union of two adjacent tiles' ranges is one
+// range: query tile q0 + 1 starts at most one tile later than q0 ends).
 __device__ __forceinline__ int next_union_tile(const Problem& p, int q0, int q1, int klim,
-                                               int last, int kt) {
-  if (p.block_mask == nullptr) return kt + 1 <= last ? kt + 1 : p.T;
-  for (++kt; kt < p.T; ++kt)
+                                               int first, int last, int kt) {
+  kt = kt + 1 < first ? first : kt + 1;
+  if (p.block_mask == nullptr) return kt <= last ? kt : p.T;
+  for (; kt <= last; ++kt)
     if (tile_live(p, q0, kt, klim) || (q1 >= 0 && tile_live(p, q1, kt, klim))) return kt;
   return p.T;
 }
@@ -101,7 +95,13 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   const int qt0 = 2 * pair;
   const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
   const int klim = key_limit(p, b);
-  const int ulast = union_last(p, qt0, qt1, klim);
+  // Live key tiles of each query tile (exact without a block mask, a bound
+  // with one) and of their union.
+  int first0, last0, first1 = 0, last1 = -1;
+  qtile_key_tiles(p, qt0, klim, first0, last0);
+  if (qt1 >= 0) qtile_key_tiles(p, qt1, klim, first1, last1);
+  const int ufirst = first0 <= last0 ? first0 : first1;
+  const int ulast = max(last0, last1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i)
@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
       bool ok = true;
-      for (int kt = next_union_tile(p, qt0, qt1, klim, ulast, -1); kt < p.T && ok;
-           kt = next_union_tile(p, qt0, qt1, klim, ulast, kt)) {
+      for (int kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, -1); kt < p.T && ok;
+           kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, kt)) {
         for (int which = 0; which < 2; ++which) {
           if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) {
             ok = false;
@@ -196,18 +196,18 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
           mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)(slot * slot_step), id_qk, 0);
       };
       // Liveness of key tile kt for query tile 0 / 1: without a block mask
-      // it is kt <= last_i, so the loop needs no predicate calls.
+      // it is first_i <= kt <= last_i, so the loop needs no predicate calls.
       const bool masked = p.block_mask != nullptr;
-      const int last0 = union_last(p, qt0, -1, klim);
-      const int last1 = qt1 >= 0 ? union_last(p, qt1, -1, klim) : -1;
-      auto live0 = [&](int kt) { return masked ? tile_live(p, qt0, kt, klim) : kt <= last0; };
+      auto live0 = [&](int kt) {
+        return masked ? tile_live(p, qt0, kt, klim) : (kt >= first0 && kt <= last0);
+      };
       auto live1 = [&](int kt) {
-        return masked ? (qt1 >= 0 && tile_live(p, qt1, kt, klim)) : kt <= last1;
+        return masked ? (qt1 >= 0 && tile_live(p, qt1, kt, klim)) : (kt >= first1 && kt <= last1);
       };
       int slot = 0, phase = 0;  // next ring slot to consume and its phase parity
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
-      int cur = next_union_tile(p, qt0, qt1, klim, ulast, -1);
+      int cur = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, -1);
       int npv0 = 0, npv1 = 0;
       if (ok && cur < p.T) {
         ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         const bool l1 = live1(cur);
         const int vslot = slot, vphase = phase;
         if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
-        const int nxt = next_union_tile(p, qt0, qt1, klim, ulast, cur);
+        const int nxt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, cur);
         const bool has_next = nxt < p.T;
         const bool n0 = has_next && live0(nxt);
         const bool n1 = has_next && live1(nxt);
@@ -288,9 +288,11 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       float m_ref = -INFINITY, l = 0.f;
       int n = 0;
       bool ok = true;
-      for (int kt = next_union_tile(p, qt0, qt1, klim, ulast, -1); kt < p.T;
-           kt = next_union_tile(p, qt0, qt1, klim, ulast, kt)) {
-        if (!tile_live(p, qt, kt, klim)) continue;
+      const int myfirst = i == 0 ? first0 : first1, mylast = i == 0 ? last0 : last1;
+      const bool bmask = p.block_mask != nullptr;
+      for (int kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, -1); kt < p.T;
+           kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, kt)) {
+        if (bmask ? !tile_live(p, qt, kt, klim) : (kt < myfirst || kt > mylast)) continue;
         if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
         tc_fence_after();
         float s[128];
@@ -300,13 +302,19 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(raw[c]);
         }
-        const bool diag = p.causal && kt == qt;
-        if (diag || (kt + 1) * 128 > klim) {
-          int lim = klim - kt * 128;
-          if (diag && r + 1 < lim) lim = r + 1;
+        // This row's allowed keys in the tile: columns [lo, hi).  Masked
+        // scores get the value that the scale sends to -inf (and that the
+        // row max / min below ignores), so p = 2^-inf = 0 for either sign.
+        {
+          const int k0 = kt * 128;
+          const int lo = row_key_lo(p, row) - k0;
+          const int hi = row_key_hi(p, row, klim) + 1 - k0;
+          if (lo > 0 || hi < 128) {
+            const float fill = cl2 >= 0.f ? -INFINITY : INFINITY;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) s[c] = -INFINITY;
+            for (int c = 0; c < 128; ++c)
+              if (c < lo || c >= hi) s[c] = fill;
+          }
         }
         // row max (row min for a negative scale): 4 independent chains of
         // 3-input max
@@ -324,8 +332,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         } else {
           float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            m4[c & 3] = fminf(m4[c & 3], s[c] == -INFINITY ? INFINITY : s[c]);
+          for (int c = 0; c < 128; ++c) m4[c & 3] = fminf(m4[c & 3], s[c]);
           const float mn = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
           mx = mn == INFINITY ? -INFINITY : mn;
         }

@@ -32,6 +32,9 @@ SIGNATURES = {
     "fa_last_device_status": ([_vp], _i),
     "fa_selftest_mma": ([_i, _vp, _vp, _vp, _i, _vp], _i),
     "fa_backward_noalloc": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
+    "fa_forward_masked": ([_vp] * 5 + [_i] * 4 + [_f, _vp, _vp], _i),
+    "fa_backward_masked": ([_vp] * 9 + [_i] * 4 + [_f, _vp, _vp, _sz, _vp], _i),
+    "fa_tile_schedule_masked": ([_i, _vp, _i, _vp, _vp, _vp, _vp], _i),
     "fa_kvcache_num_splits": ([_i] * 6, _i),
     "fa_kvcache_workspace_bytes": ([_i] * 6, _sz),
     "fa_forward_kvcache": ([_vp] * 5 + [_i] * 5 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
@@ -42,6 +45,13 @@ KVCACHE_MAX_SPLITS = 256  # FA_KVCACHE_MAX_SPLITS (include/fa_kvcache.h)
 
 # Size of the library's built-in backward scratch (include/fa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+class Mask(ctypes.Structure):
+    """``fa_mask`` of include/fa.h: every mask option of the *_masked calls."""
+    _fields_ = [("causal", ctypes.c_int), ("window_left", ctypes.c_int),
+                ("window_right", ctypes.c_int), ("block_mask", ctypes.c_void_p),
+                ("kv_len", ctypes.c_void_p)]
 
 
 class FAError(RuntimeError):
@@ -103,20 +113,29 @@ def _mask_args(N, block_mask, kv_len, B):
     return _ptr(block_mask), _ptr(kv_len)
 
 
+def _mask(N, causal, block_mask, kv_len, B, window):
+    bm, kl = _mask_args(N, block_mask, kv_len, B)
+    wl, wr = (-1, -1) if window is None else (
+        -1 if window[0] is None else int(window[0]), -1 if window[1] is None else int(window[1]))
+    return Mask(int(bool(causal)), wl, wr, bm, kl)
+
+
 def forward(q, k, v, causal=False, block_mask=None, kv_len=None, scale=None,
-            out=None, lse=None, stream=None):
-    """O, LSE = attention(q, k, v); see include/fa.h ``fa_forward``."""
+            out=None, lse=None, stream=None, window=None):
+    """O, LSE = attention(q, k, v); see include/fa.h ``fa_forward_masked``.
+    ``window`` = (left, right): key j allowed for query i only if
+    i - left <= j <= i + right (None or negative = unbounded side)."""
     lib = load()
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
-    bm, kl = _mask_args(N, block_mask, kv_len, B)
-    st = lib.fa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
-                        scale, int(bool(causal)), bm, kl, _stream(stream))
+    m = _mask(N, causal, block_mask, kv_len, B, window)
+    st = lib.fa_forward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                               scale, ctypes.byref(m), _stream(stream))
     if st != FA_OK:
-        raise FAError(st, "fa_forward")
+        raise FAError(st, "fa_forward_masked")
     return out, lse
 
 
@@ -125,8 +144,8 @@ def backward_workspace_bytes(B, H, N, d):
 
 
 def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
-             scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
-    """dQ, dK, dV of sum(O * dO); see include/fa.h ``fa_backward``."""
+             scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None, window=None):
+    """dQ, dK, dV of sum(O * dO); see include/fa.h ``fa_backward_masked``."""
     lib = load()
     _check_qkv(q, k, v, o, do)
     B, H, N, d = q.shape
@@ -137,13 +156,13 @@ def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    bm, kl = _mask_args(N, block_mask, kv_len, B)
-    st = lib.fa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
-                         _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, scale,
-                         int(bool(causal)), bm, kl, _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream))
+    m = _mask(N, causal, block_mask, kv_len, B, window)
+    st = lib.fa_backward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, scale,
+                                ctypes.byref(m), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
     if st != FA_OK:
-        raise FAError(st, "fa_backward")
+        raise FAError(st, "fa_backward_masked")
     return dq, dk, dv
 
 
@@ -233,19 +252,20 @@ def combine(o_parts, lse_parts, out=None, lse=None, stream=None):
     return out, lse
 
 
-def tile_schedule(N, causal=False, block_mask=None, kv_len=None, b=0, device="cuda"):
-    """(row_ptr, col_idx, partial) CUDA tensors; see ``fa_tile_schedule``."""
+def tile_schedule(N, causal=False, block_mask=None, kv_len=None, b=0, device="cuda",
+                  window=None):
+    """(row_ptr, col_idx, partial) CUDA tensors; see ``fa_tile_schedule_masked``."""
     lib = load()
     T = (N + 127) // 128
     B = 0 if kv_len is None else kv_len.shape[0]
-    bm, kl = _mask_args(N, block_mask, kv_len, B)
+    m = _mask(N, causal, block_mask, kv_len, B, window)
     row_ptr = torch.zeros(T + 1, device=device, dtype=torch.int32)
     col_idx = torch.full((T * T,), -1, device=device, dtype=torch.int32)
     partial = torch.full((T * T,), 255, device=device, dtype=torch.uint8)
-    st = lib.fa_tile_schedule(N, int(bool(causal)), bm, kl, b, _ptr(row_ptr),
-                              _ptr(col_idx), _ptr(partial), _stream())
+    st = lib.fa_tile_schedule_masked(N, ctypes.byref(m), b, _ptr(row_ptr),
+                                     _ptr(col_idx), _ptr(partial), _stream())
     if st != FA_OK:
-        raise FAError(st, "fa_tile_schedule")
+        raise FAError(st, "fa_tile_schedule_masked")
     return row_ptr, col_idx, partial
 
 

@@ -22,8 +22,14 @@
  *     (!causal || j <= i)
  *  && (block_mask == NULL || block_mask[(i/128)*T + j/128] != 0)
  *  && (kv_len == NULL     || j < kv_len[b])              (kv_len clamped to [0, N])
+ *  && (window_left  < 0   || j >= i - window_left)       (fa_mask calls only)
+ *  && (window_right < 0   || j <= i + window_right)      (fa_mask calls only)
  * with T = ceil(N/128).  A query row with no allowed key gets O = 0 and
- * LSE = -inf, and contributes nothing to the gradients.
+ * LSE = -inf, and contributes nothing to the gradients.  The sliding window
+ * follows page "FlashAttention" (aiwiki), section "Software integration and
+ * limitations", which lists causal and sliding-window masks among the
+ * method's interfaces; (w, 0) with causal is the usual causal window of the
+ * last w+1 keys.
  *
  * Common conventions
  *  - Tensors are dense, row-major, on the current CUDA device:
@@ -70,11 +76,30 @@ typedef enum {
 FA_API const char* fa_status_string(int status);
 
 /*
+ * Every mask option in one place (the fa_*_masked calls take a pointer to
+ * it; NULL = no mask).  Fields as in the allowed-pair rule above:
+ *   causal        nonzero = j <= i
+ *   window_left   >= 0: j >= i - window_left;  < 0: unbounded
+ *   window_right  >= 0: j <= i + window_right; < 0: unbounded
+ *   block_mask    uint8 [T, T] device or NULL (zero tiles are skipped)
+ *   kv_len        int32 [B] device or NULL
+ * A window side of N or more is the same as unbounded.
+ */
+typedef struct fa_mask {
+  int causal;
+  int window_left;
+  int window_right;
+  const uint8_t* block_mask;
+  const int32_t* kv_len;
+} fa_mask;
+
+/*
  * Forward pass: O and LSE.
  *   q, k, v    : bf16 [B,H,N,d], read only.
  *   o          : bf16 [B,H,N,d], written.
  *   lse        : fp32 [B,H,N], written (natural log; -inf on fully masked rows).
- *   scale      : multiplies Q K^T (usually 1/sqrt(d)); any finite value.
+ *   scale      : multiplies Q K^T (usually 1/sqrt(d)); any finite value, of
+ *                either sign (0 gives uniform weights over the allowed keys).
  *   causal     : nonzero = causal mask j <= i.
  *   block_mask : see above; its zero tiles are never loaded or computed.
  *   kv_len     : see above.
@@ -83,6 +108,11 @@ FA_API const char* fa_status_string(int status);
 FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                int B, int H, int N, int d, float scale, int causal,
                const uint8_t* block_mask, const int32_t* kv_len, void* stream);
+
+/* fa_forward with the full mask description (sliding windows included). */
+FA_API int fa_forward_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int d, float scale, const fa_mask* mask,
+                             void* stream);
 
 /*
  * Bytes of device workspace fa_backward needs: LSE*log2(e) and D
@@ -112,6 +142,13 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
                 int B, int H, int N, int d, float scale, int causal,
                 const uint8_t* block_mask, const int32_t* kv_len,
                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa_backward with the full mask description; the mask must be the one the
+ * forward was called with. */
+FA_API int fa_backward_masked(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, float scale, const fa_mask* mask,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The three launches of fa_backward, exposed one by one so a caller can
@@ -187,6 +224,10 @@ FA_API int fa_backward_noalloc(const void* q, const void* k, const void* v, cons
 FA_API int fa_tile_schedule(int N, int causal, const uint8_t* block_mask,
                      const int32_t* kv_len, int b, int32_t* row_ptr,
                      int32_t* col_idx, uint8_t* partial, void* stream);
+
+/* fa_tile_schedule with the full mask description. */
+FA_API int fa_tile_schedule_masked(int N, const fa_mask* mask, int b, int32_t* row_ptr,
+                                   int32_t* col_idx, uint8_t* partial, void* stream);
 
 /*
  * Reads and clears the library's device error word on the current device

@@ -8,11 +8,16 @@ inputs, fp32 accumulation):
   LSE         : max |gpu - ref| <= 1e-3 on rows with an allowed key;
                 exactly -inf (and O == 0) on rows without one.
 
-When a reference tensor is identically zero (e.g. dQ with a single key,
-where dS = P (dP - D) vanishes), the relative bound has nothing to scale;
-the bound then uses max |ref| floored at ABS_FLOOR = 1e-4 (inputs are
-N(0, 1), so 1e-4 sits far below every nonzero reference magnitude in the
-tests and far above the fp32 rounding noise such a zero picks up).
+When a reference tensor is identically zero (dQ and dK when every row has a
+single allowed key, where dS = P (dP - D) vanishes), the relative bound has
+nothing to scale; the bound then uses max |ref| floored at ABS_FLOOR.  The
+floor comes from the arithmetic of that cancellation: dP_ij and D_i are two
+fp32 dot products of d bf16 products of N(0, 1) values (magnitude
+sum_c |dO_c V_c| ~ 0.64 d ~ 80 at d = 128), each off by about sqrt(d) * 2^-24
+times that (~5e-5), so dS ~ 5e-5 and dQ = scale * dS K ~ 0.09 * 5e-5 * 3
+~ 1e-5.  ABS_FLOOR = 1e-3 puts the bound (2e-5 for gradients) above that
+noise and still two orders of magnitude below every nonzero gradient
+magnitude in the tests (max |dQ| is O(0.1) or more).
 """
 
 import numpy as np
@@ -22,7 +27,7 @@ from exact_io_aware_tma_gb300 import fa
 from exact_io_aware_tma_gb300.workloads import to_f64
 
 TOL_O, TOL_GRAD, TOL_LSE = 1e-2, 2e-2, 1e-3
-ABS_FLOOR = 1e-4
+ABS_FLOOR = 1e-3
 
 
 def to_device(inp, dev="cuda"):
@@ -37,7 +42,7 @@ def to_device(inp, dev="cuda"):
 def run_gpu(inp, backward=True):
     g = to_device(inp)
     kw = dict(causal=g["causal"], block_mask=g["block_mask"], kv_len=g["kv_len"],
-              scale=g["scale"])
+              scale=g["scale"], window=inp.get("window"))
     o, lse = fa.forward(g["q"], g["k"], g["v"], **kw)
     res = dict(o=o, lse=lse)
     if backward:

@@ -24,7 +24,7 @@ def oracle_on_heads(inp, heads):
         kv = None if inp["kv_len"] is None else inp["kv_len"][b:b + 1]
         sl = (slice(b, b + 1), slice(h, h + 1))
         r = attention_backward(q[sl], k[sl], v[sl], do[sl], inp["scale"], inp["causal"],
-                               inp["block_mask"], kv)
+                               inp["block_mask"], kv, window=inp.get("window"))
         for arr, val in zip(out, (r[0], r[1], r[2], r[3], r[4])):
             arr[b, h] = val[0, 0]
     return tuple(out)
