@@ -65,6 +65,67 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same preprocess for the packed variable-length layout: row `row` of
+// (b, h) is token cu_seqlens[b] + row of [total][H][d] (rows at or past the
+// sequence's length are padding); LSE is [H][total].  The fp32 dQ
+// accumulator [total][H][d] is cleared in full, so tokens outside every
+// sequence end with dQ = 0.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_packed_kernel(const __nv_bfloat16* __restrict__ o,
+                                 const __nv_bfloat16* __restrict__ dout,
+                                 const float* __restrict__ lse, float* __restrict__ lse2,
+                                 float* __restrict__ dvec, float* __restrict__ dq_acc,
+                                 const int32_t* __restrict__ cu, int H, long long heads, int total,
+                                 int maxlen, int npad) {
+  constexpr int CH = D / 8;
+  const long long n = heads * npad * CH;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n;
+       i += stride) {
+    float acc = 0.f;
+    const bool in = i < n;
+    const long long prow = i / CH;  // padded row index
+    const long long bh = prow / npad;
+    const int row = (int)(prow % npad);
+    int start = 0, len = 0;
+    if (in) {
+      const int b = (int)(bh / H);
+      int s0 = __ldg(cu + b), e0 = __ldg(cu + b + 1);
+      s0 = min(max(s0, 0), total);
+      e0 = min(max(e0, s0), total);
+      start = s0;
+      len = min(e0 - s0, maxlen);
+    }
+    const int h = (int)(bh % H);
+    const bool live = in && row < len;
+    if (live) {
+      const long long e = (((long long)(start + row) * H + h) * CH + (i % CH)) * 8;
+      uint4 a = *reinterpret_cast<const uint4*>(o + e);
+      uint4 b4 = *reinterpret_cast<const uint4*>(dout + e);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float2 x = __bfloat1622float2(pa[j]);
+        float2 y = __bfloat1622float2(pb[j]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = CH / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in && (i % CH) == 0) {
+      dvec[prow] = live ? acc : 0.f;
+      const float l = live ? lse[(long long)h * total + start + row] : -INFINITY;
+      lse2[prow] = l == -INFINITY ? INFINITY : l * kLog2e;
+    }
+  }
+  const long long nz = (long long)total * H * D / 4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nz; i += stride)
+    reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // dQ = scale * dQacc, fp32 -> bf16, 8 elements per thread.
 __global__ void __launch_bounds__(256)
     dq_convert_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
@@ -170,6 +231,8 @@ static int check_sizes(int B, int H, int N, int d, float scale, const fa_mask* m
   p->block_mask = m != nullptr ? m->block_mask : nullptr;
   p->kv_len = m != nullptr ? m->kv_len : nullptr;
   p->status = nullptr;
+  p->cu_seqlens = nullptr;
+  p->total = 0;
   return FA_OK;
 }
 
@@ -382,6 +445,94 @@ int fa_tile_schedule(int N, int causal, const uint8_t* block_mask, const int32_t
                      void* stream) {
   const fa_mask m = plain_mask(causal, block_mask, kv_len);
   return fa_tile_schedule_masked(N, &m, b, row_ptr, col_idx, partial, stream);
+}
+
+// ---------------------------------------------------------------- packed
+// Variable-length sequences in the packed layout (include/fa.h): the grid is
+// sized by max_seqlen and each CTA takes its own sequence's span.
+
+static int check_varlen(int B, int H, int total, int max_seqlen, int d, float scale,
+                        const fa_mask* mask, const int32_t* cu, Problem* p) {
+  if (B < 1 || H < 1 || total < 1 || max_seqlen < 1) return FA_ERR_INVALID_ARG;
+  if (mask != nullptr && (mask->block_mask != nullptr || mask->kv_len != nullptr))
+    return FA_ERR_UNSUPPORTED;
+  if (cu == nullptr || !aligned(cu, 4)) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 2147483647LL) return FA_ERR_INVALID_ARG;
+  if ((double)total * H * d > 4.0e18) return FA_ERR_INVALID_ARG;
+  int st = check_sizes(B, H, max_seqlen, d, scale, mask, p);
+  if (st != FA_OK) return st;
+  p->cu_seqlens = cu;
+  p->total = total;
+  return FA_OK;
+}
+
+size_t fa_varlen_workspace_bytes(int B, int H, int total, int max_seqlen, int d) {
+  Problem p;
+  int dummy = 0;
+  if (check_varlen(B, H, total, max_seqlen, d, 1.0f, nullptr, &dummy, &p) != FA_OK) return 0;
+  const size_t vec = round_up((size_t)B * H * padded_rows(max_seqlen) * sizeof(float), 256);
+  return 2 * vec + round_up((size_t)total * H * d * sizeof(float), 256);
+}
+
+int fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const int32_t* cu_seqlens, int B, int H, int total, int max_seqlen, int d,
+                      float scale, const fa_mask* mask, void* stream) {
+  Problem p;
+  int st = check_varlen(B, H, total, max_seqlen, d, scale, mask, cu_seqlens, &p);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  p.status = status_word();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  cudaError_t e = launch_fwd_tc(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       const int32_t* cu_seqlens, int B, int H, int total, int max_seqlen, int d,
+                       float scale, const fa_mask* mask, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  Problem p;
+  int st = check_varlen(B, H, total, max_seqlen, d, scale, mask, cu_seqlens, &p);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < fa_varlen_workspace_bytes(B, H, total, max_seqlen, d))
+    return FA_ERR_INVALID_ARG;
+  p.status = status_word();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long heads = (long long)B * H;
+  const int npad = padded_rows(max_seqlen);
+  const size_t vec = round_up((size_t)heads * npad * sizeof(float), 256);
+  float* lse2 = static_cast<float*>(workspace);
+  float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + vec);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * vec);
+  const unsigned nblk = elementwise_blocks(heads * npad * (d / 8));
+  auto ob = static_cast<const __nv_bfloat16*>(o);
+  auto db = static_cast<const __nv_bfloat16*>(dout);
+  if (d == 64)
+    bwd_preprocess_packed_kernel<64><<<nblk, 256, 0, s>>>(ob, db, lse, lse2, dvec, dq_acc,
+                                                          cu_seqlens, H, heads, total,
+                                                          max_seqlen, npad);
+  else
+    bwd_preprocess_packed_kernel<128><<<nblk, 256, 0, s>>>(ob, db, lse, lse2, dvec, dq_acc,
+                                                           cu_seqlens, H, heads, total,
+                                                           max_seqlen, npad);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  cudaError_t e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  const long long chunks = (long long)total * H * (d / 8);
+  dq_convert_kernel<<<elementwise_blocks(chunks), 256, 0, s>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), scale, chunks);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_last_device_status(void* stream) {

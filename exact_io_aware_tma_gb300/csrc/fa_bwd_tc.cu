@@ -92,14 +92,33 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, 
   return false;
 }
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                  Problem p, const float* __restrict__ lse2, const float* __restrict__ dvec,
-                  float* __restrict__ dq_acc, int npad) {
+                  const Problem pin, const float* __restrict__ lse2, const float* __restrict__ dvec,
+                  float* __restrict__ dq_acc, int npad, __nv_bfloat16* __restrict__ dk_rows,
+                  __nv_bfloat16* __restrict__ dv_rows) {
   using C = BwdTc<D>;
+  // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
+  // (x, row, bh)), or one sequence of the packed layout [total][H][d]
+  // (coordinates (x, h, start + row)), whose length then plays the role of N.
+  const long long bh = blockIdx.x;
+  const int kt = blockIdx.y;  // small key tiles carry the most causal work: first
+  const int b = (int)(bh / pin.H);
+  const int head = (int)(bh % pin.H);
+  Problem p = pin;
+  int start = 0;
+  if constexpr (PACKED) {
+    int len;
+    seq_span(pin, b, start, len);
+    p.N = len;
+    p.T = (len + kTile - 1) / kTile;
+  }
+  if (kt >= p.T) return;  // packed: past this sequence's key tiles
+  auto cy = [&](int row) { return PACKED ? head : row; };
+  auto cz = [&](int row) { return PACKED ? start + row : (int)bh; };
   extern __shared__ uint8_t smem_raw[];
   // An offset (not an integer round trip) keeps the pointer visibly in shared
   // memory, so C++ accesses through it compile to shared-memory instructions.
@@ -112,9 +131,6 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   const Abort ab{abort_flag, p.status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long bh = blockIdx.x;
-  const int kt = blockIdx.y;  // small key tiles carry the most causal work: first
-  const int b = (int)(bh / p.H);
   const int klim = key_limit(p, b);
 
   if (threadIdx.x == 0) {
@@ -146,8 +162,10 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     if (lane == 0) {
       mbar_expect_tx(bar(C::B_KV), 2 * C::KT);
       for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(s0 + C::OFF_K + h * C::HALF_K, &tm_k, bar(C::B_KV), h * 64, kt * 128, (int)bh);
-        tma_load_3d(s0 + C::OFF_V + h * C::HALF_K, &tm_v, bar(C::B_KV), h * 64, kt * 128, (int)bh);
+        tma_load_3d(s0 + C::OFF_K + h * C::HALF_K, &tm_k, bar(C::B_KV), h * 64, cy(kt * 128),
+                    cz(kt * 128));
+        tma_load_3d(s0 + C::OFF_V + h * C::HALF_K, &tm_v, bar(C::B_KV), h * 64, cy(kt * 128),
+                    cz(kt * 128));
       }
       int qt = -1, sub = 0, slot = 0, round = 0;
       while (next_q_step(p, kt, klim, qt, sub)) {
@@ -158,8 +176,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
         const uint32_t vb = s0 + C::OFF_VEC + slot * 512;
         mbar_expect_tx(fb, 2 * C::QB + 512);
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(st + h * C::HALF_Q, &tm_q, fb, h * 64, q0, (int)bh);
-          tma_load_3d(st + C::QB + h * C::HALF_Q, &tm_do, fb, h * 64, q0, (int)bh);
+          tma_load_3d(st + h * C::HALF_Q, &tm_q, fb, h * 64, cy(q0), cz(q0));
+          tma_load_3d(st + C::QB + h * C::HALF_Q, &tm_do, fb, h * 64, cy(q0), cz(q0));
         }
         bulk_load(vb, lse2 + vec_base + q0, 256, fb);
         bulk_load(vb + 256, dvec + vec_base + q0, 256, fb);
@@ -342,10 +360,14 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_EW + bf));
     }
-    // ---- epilogue: dK (x scale), dV -> bf16 -> shared (swizzled) -> TMA store
+    // ---- epilogue: dK (x scale), dV -> bf16 -> shared (swizzled) -> TMA store;
+    // in the packed layout a key tile that ends past its sequence is written
+    // row by row instead (a whole-tile store would overwrite the next
+    // sequence's first rows).
     if (ok) ok = mbar_wait(bar(C::B_FIN), 0, ab);
     tc_fence_after();
     uint8_t* stg = smem + C::OFF_ST;  // dK tile, then dV tile
+    const bool direct = PACKED && (kt + 1) * 128 > p.N;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const uint32_t col = t == 0 ? C::COL_DK : C::COL_DV;
@@ -366,18 +388,26 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int cc = 4 * c + q;
-          uint8_t* dst = stg + t * C::KT + (cc >> 3) * C::HALF_K + r * 128 +
-                         (((cc & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          const uint4 w = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+          if (direct) {
+            if (ok && j < p.N)
+              reinterpret_cast<uint4*>((t == 0 ? dk_rows : dv_rows) +
+                                       ((size_t)(start + j) * p.H + head) * D)[cc] = w;
+          } else {
+            uint8_t* dst = stg + t * C::KT + (cc >> 3) * C::HALF_K + r * 128 +
+                           (((cc & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = w;
+          }
         }
       }
     }
     fence_proxy_async_smem();
     named_barrier(1, 128);
-    if (ok && r == 0) {
+    if (ok && r == 0 && !direct) {
       for (int h = 0; h < D / 64; ++h) {
-        tma_store_3d(&tm_dk, smem_u32(stg) + h * C::HALF_K, h * 64, kt * 128, (int)bh);
-        tma_store_3d(&tm_dv, smem_u32(stg) + C::KT + h * C::HALF_K, h * 64, kt * 128, (int)bh);
+        tma_store_3d(&tm_dk, smem_u32(stg) + h * C::HALF_K, h * 64, cy(kt * 128), cz(kt * 128));
+        tma_store_3d(&tm_dv, smem_u32(stg) + C::KT + h * C::HALF_K, h * 64, cy(kt * 128),
+                     cz(kt * 128));
       }
       tma_store_commit();
       tma_store_wait_all();
@@ -403,10 +433,13 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       // query the warp's 32 lanes add 32 consecutive floats of its row.
       if (valid) {
         const int rows = min(64, p.N - q0);
-        float* dst = dq_acc + ((size_t)bh * p.N + q0) * D + c;
+        // padded: [B*H][N][d]; packed: [total][H][d]
+        const size_t row_stride = PACKED ? (size_t)p.H * D : (size_t)D;
+        float* dst = PACKED ? dq_acc + ((size_t)(start + q0) * p.H + head) * D + c
+                            : dq_acc + ((size_t)bh * p.N + q0) * D + c;
 #pragma unroll
         for (int q = 0; q < 64; ++q)
-          if (q < rows) atomicAdd(dst + (size_t)q * D, __uint_as_float(v[q]));
+          if (q < rows) atomicAdd(dst + (size_t)q * row_stride, __uint_as_float(v[q]));
       }
     }
   }
@@ -418,32 +451,48 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool PACKED>
 static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
                                    const void* dout, const float* lse2, const float* dvec,
                                    float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
   using C = BwdTc<D>;
   const long long bh = (long long)p.B * p.H;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) || !make_bf16_map_3d(&tk, k, D, p.N, bh, 128) ||
-      !make_bf16_map_3d(&tv, v, D, p.N, bh, 128) ||
-      !make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) ||
-      !make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) || !make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128))
-    return cudaErrorInvalidValue;
-  auto kern = bwd_tc_kernel<D>;
+  bool maps;
+  if constexpr (PACKED)
+    maps = make_bf16_map_packed(&tq, q, D, p.H, p.total, C::BQ) &&
+           make_bf16_map_packed(&tk, k, D, p.H, p.total, 128) &&
+           make_bf16_map_packed(&tv, v, D, p.H, p.total, 128) &&
+           make_bf16_map_packed(&tdo, dout, D, p.H, p.total, C::BQ) &&
+           make_bf16_map_packed(&tdk, dk, D, p.H, p.total, 128) &&
+           make_bf16_map_packed(&tdv, dv, D, p.H, p.total, 128);
+  else
+    maps = make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) &&
+           make_bf16_map_3d(&tk, k, D, p.N, bh, 128) && make_bf16_map_3d(&tv, v, D, p.N, bh, 128) &&
+           make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) &&
+           make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) && make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128);
+  if (!maps) return cudaErrorInvalidValue;
+  auto kern = bwd_tc_kernel<D, PACKED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)bh, (unsigned)p.T);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad,
+                                          static_cast<__nv_bfloat16*>(dk),
+                                          static_cast<__nv_bfloat16*>(dv));
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
                           void* dk, void* dv, int npad, cudaStream_t st) {
-  return p.d == 64 ? launch_bwd_tc_t<64>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
-                   : launch_bwd_tc_t<128>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st);
+  if (p.cu_seqlens != nullptr)
+    return p.d == 64
+               ? launch_bwd_tc_t<64, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
+               : launch_bwd_tc_t<128, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st);
+  return p.d == 64
+             ? launch_bwd_tc_t<64, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
+             : launch_bwd_tc_t<128, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st);
 }
 
 }  // namespace fa

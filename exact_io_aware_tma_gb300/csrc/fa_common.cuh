@@ -24,7 +24,26 @@ struct Problem {
   const uint8_t* block_mask;  // [T, T] or nullptr
   const int32_t* kv_len;      // [B] or nullptr
   int* status;                // device error word (bounded waits record here)
+  // Packed variable-length layout (kernels instantiated for it only): the B
+  // sequences lie back to back in [total, H, d]; sequence b is tokens
+  // cu_seqlens[b] .. cu_seqlens[b+1]-1, and N above is the longest length
+  // (it sizes the grid; each CTA takes its own sequence's length as N).
+  const int32_t* cu_seqlens;
+  int total;
 };
+
+// Token span of sequence b in the packed layout.  Offsets that are out of
+// order, out of range or longer than N are clamped (the call then records
+// FA_ERR_INVALID_ARG in the status word).
+__device__ __forceinline__ void seq_span(const Problem& p, int b, int& start, int& len) {
+  int s = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
+  const bool bad = s < 0 || e < s || e > p.total || e - s > p.N;
+  s = min(max(s, 0), p.total);
+  e = min(max(e, s), p.total);
+  start = s;
+  len = min(e - s, p.N);
+  if (bad && threadIdx.x == 0 && p.status != nullptr) atomicExch(p.status, 1);
+}
 
 // Valid-key bound of batch element b: min(N, max(0, kv_len[b])).
 __device__ __forceinline__ int key_limit(const Problem& p, int b) {

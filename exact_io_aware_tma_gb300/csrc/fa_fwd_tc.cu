@@ -70,12 +70,30 @@ __device__ __forceinline__ int next_union_tile(const Problem& p, int q0, int q1,
   return p.T;
 }
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  Problem p, float* __restrict__ lse) {
+                  const Problem pin, float* __restrict__ lse, __nv_bfloat16* __restrict__ o_rows) {
   using C = FwdTc<D>;
+  // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
+  // (x, row, bh)), or one sequence of the packed layout [total][H][d]
+  // (coordinates (x, h, start + row)), whose length then plays the role of N.
+  const long long bh = blockIdx.x;
+  const int b = (int)(bh / pin.H);
+  const int head = (int)(bh % pin.H);
+  Problem p = pin;
+  int start = 0;
+  if constexpr (PACKED) {
+    int len;
+    seq_span(pin, b, start, len);
+    p.N = len;
+    p.T = (len + kTile - 1) / kTile;
+  }
+  const int npairs = (p.T + 1) / 2;
+  if ((int)blockIdx.y >= npairs) return;  // packed: past this sequence's tiles
+  auto cy = [&](int row) { return PACKED ? head : row; };
+  auto cz = [&](int row) { return PACKED ? start + row : (int)bh; };
   extern __shared__ uint8_t smem_raw[];
   // An offset (not an integer round trip) keeps the pointer visibly in shared
   // memory, so C++ accesses through it compile to shared-memory instructions.
@@ -88,10 +106,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   const Abort ab{abort_flag, p.status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int npairs = (p.T + 1) / 2;
   const int pair = npairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
-  const long long bh = blockIdx.x;
-  const int b = (int)(bh / p.H);
   const int qt0 = 2 * pair;
   const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
   const int klim = key_limit(p, b);
@@ -129,10 +144,11 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     if (lane == 0) {
       mbar_expect_tx(bar(C::B_Q), (qt1 >= 0 ? 2 : 1) * C::TILE);
       for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(s0 + C::OFF_Q + h * C::HALF, &tm_q, bar(C::B_Q), h * 64, qt0 * 128, (int)bh);
+        tma_load_3d(s0 + C::OFF_Q + h * C::HALF, &tm_q, bar(C::B_Q), h * 64, cy(qt0 * 128),
+                    cz(qt0 * 128));
         if (qt1 >= 0)
           tma_load_3d(s0 + C::OFF_Q + C::TILE + h * C::HALF, &tm_q, bar(C::B_Q), h * 64,
-                      qt1 * 128, (int)bh);
+                      cy(qt1 * 128), cz(qt1 * 128));
       }
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
@@ -148,7 +164,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
           mbar_expect_tx(bar(C::B_FULL + slot), C::TILE);
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(dst + h * C::HALF, which == 0 ? &tm_k : &tm_v, bar(C::B_FULL + slot),
-                        h * 64, kt * 128, (int)bh);
+                        h * 64, cy(kt * 128), cz(kt * 128));
           if (++slot == C::NSLOT) {
             slot = 0;
             ++round;
@@ -378,11 +394,15 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         if (lane == 0) mbar_arrive(bar(C::B_P + i));
         ++n;
       }
-      // ---- epilogue: O = u / l -> bf16 -> shared (swizzled) -> TMA store
+      // ---- epilogue: O = u / l -> bf16 -> shared (swizzled) -> TMA store;
+      // in the packed layout a tile that ends past its sequence is written
+      // row by row instead (a whole-tile store would overwrite the next
+      // sequence's first rows).
       if (ok) ok = mbar_wait(bar(C::B_O + i), 0, ab);
       tc_fence_after();
       uint8_t* stage = smem + C::OFF_Q + i * C::TILE;
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool direct = PACKED && (qt + 1) * 128 > p.N;
       if (ok) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -396,18 +416,26 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int cc = 4 * c + q;
-            uint8_t* dst = stage + (cc >> 3) * C::HALF + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            const uint4 w = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            if (direct) {
+              if (row < p.N)
+                reinterpret_cast<uint4*>(o_rows + ((size_t)(start + row) * p.H + head) * D)[cc] = w;
+            } else {
+              uint8_t* dst = stage + (cc >> 3) * C::HALF + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(dst) = w;
+            }
           }
         }
-        if (row < p.N)
-          lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        if (row < p.N) {
+          const size_t li = PACKED ? (size_t)head * p.total + start + row : (size_t)bh * p.N + row;
+          lse[li] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        }
       }
       fence_proxy_async_smem();
       named_barrier(1 + i, 128);
-      if (ok && r == 0) {
+      if (ok && r == 0 && !direct) {
         for (int h = 0; h < D / 64; ++h)
-          tma_store_3d(&tm_o, smem_u32(stage) + h * C::HALF, h * 64, qt * 128, (int)bh);
+          tma_store_3d(&tm_o, smem_u32(stage) + h * C::HALF, h * 64, cy(qt * 128), cz(qt * 128));
         tma_store_commit();
         tma_store_wait_all();
       }
@@ -421,28 +449,39 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool PACKED>
 static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
                                    void* o, float* lse, cudaStream_t st) {
   using C = FwdTc<D>;
   const long long bh = (long long)p.B * p.H;
   CUtensorMap tq, tk, tv, to;
-  if (!make_bf16_map_3d(&tq, q, D, p.N, bh, 128) || !make_bf16_map_3d(&tk, k, D, p.N, bh, 128) ||
-      !make_bf16_map_3d(&tv, v, D, p.N, bh, 128) || !make_bf16_map_3d(&to, o, D, p.N, bh, 128))
-    return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D>;
+  bool maps;
+  if constexpr (PACKED)
+    maps = make_bf16_map_packed(&tq, q, D, p.H, p.total, 128) &&
+           make_bf16_map_packed(&tk, k, D, p.H, p.total, 128) &&
+           make_bf16_map_packed(&tv, v, D, p.H, p.total, 128) &&
+           make_bf16_map_packed(&to, o, D, p.H, p.total, 128);
+  else
+    maps = make_bf16_map_3d(&tq, q, D, p.N, bh, 128) && make_bf16_map_3d(&tk, k, D, p.N, bh, 128) &&
+           make_bf16_map_3d(&tv, v, D, p.N, bh, 128) && make_bf16_map_3d(&to, o, D, p.N, bh, 128);
+  if (!maps) return cudaErrorInvalidValue;
+  auto kern = fwd_tc_kernel<D, PACKED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)bh, (unsigned)((p.T + 1) / 2));
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, to, p, lse);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, to, p, lse,
+                                          static_cast<__nv_bfloat16*>(o));
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, cudaStream_t st) {
-  return p.d == 64 ? launch_fwd_tc_t<64>(p, q, k, v, o, lse, st)
-                   : launch_fwd_tc_t<128>(p, q, k, v, o, lse, st);
+  if (p.cu_seqlens != nullptr)
+    return p.d == 64 ? launch_fwd_tc_t<64, true>(p, q, k, v, o, lse, st)
+                     : launch_fwd_tc_t<128, true>(p, q, k, v, o, lse, st);
+  return p.d == 64 ? launch_fwd_tc_t<64, false>(p, q, k, v, o, lse, st)
+                   : launch_fwd_tc_t<128, false>(p, q, k, v, o, lse, st);
 }
 
 }  // namespace fa

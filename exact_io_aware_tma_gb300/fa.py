@@ -35,6 +35,9 @@ SIGNATURES = {
     "fa_forward_masked": ([_vp] * 5 + [_i] * 4 + [_f, _vp, _vp], _i),
     "fa_backward_masked": ([_vp] * 9 + [_i] * 4 + [_f, _vp, _vp, _sz, _vp], _i),
     "fa_tile_schedule_masked": ([_i, _vp, _i, _vp, _vp, _vp, _vp], _i),
+    "fa_forward_varlen": ([_vp] * 6 + [_i] * 5 + [_f, _vp, _vp], _i),
+    "fa_varlen_workspace_bytes": ([_i] * 5, _sz),
+    "fa_backward_varlen": ([_vp] * 10 + [_i] * 5 + [_f, _vp, _vp, _sz, _vp], _i),
     "fa_kvcache_num_splits": ([_i] * 6, _i),
     "fa_kvcache_workspace_bytes": ([_i] * 6, _sz),
     "fa_forward_kvcache": ([_vp] * 5 + [_i] * 5 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
@@ -186,6 +189,69 @@ def backward_noalloc(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=
                                  int(bool(causal)), bm, kl, _stream(stream))
     if st != FA_OK:
         raise FAError(st, "fa_backward_noalloc")
+    return dq, dk, dv
+
+
+def _check_packed(*ts):
+    ref = ts[0]
+    for t in ts:
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 3):
+            raise ValueError("packed tensors must be contiguous [total, H, d] bf16 CUDA tensors")
+        if t.shape != ref.shape:
+            raise ValueError("packed tensors must share one [total, H, d] shape")
+
+
+def _check_cu(cu_seqlens):
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32
+            and cu_seqlens.is_contiguous() and cu_seqlens.dim() == 1 and cu_seqlens.numel() >= 2):
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA [B+1] tensor")
+    return cu_seqlens.numel() - 1
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, window=None, scale=None,
+                   out=None, lse=None, stream=None):
+    """O [total,H,d], LSE [H,total] of packed sequences; see ``fa_forward_varlen``."""
+    lib = load()
+    _check_packed(q, k, v)
+    B = _check_cu(cu_seqlens)
+    total, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), device=q.device, dtype=torch.float32) if lse is None else lse
+    m = _mask(1, causal, None, None, 0, window)
+    st = lib.fa_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+                               B, H, total, int(max_seqlen), d, scale, ctypes.byref(m),
+                               _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_forward_varlen")
+    return out, lse
+
+
+def varlen_workspace_bytes(B, H, total, max_seqlen, d):
+    return int(load().fa_varlen_workspace_bytes(B, H, total, max_seqlen, d))
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, window=None,
+                    scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV [total,H,d] of packed sequences; see ``fa_backward_varlen``."""
+    lib = load()
+    _check_packed(q, k, v, o, do)
+    B = _check_cu(cu_seqlens)
+    total, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = varlen_workspace_bytes(B, H, total, int(max_seqlen), d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    m = _mask(1, causal, None, None, 0, window)
+    st = lib.fa_backward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B, H, total,
+                                int(max_seqlen), d, scale, ctypes.byref(m), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_backward_varlen")
     return dq, dk, dv
 
 

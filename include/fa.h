@@ -230,6 +230,47 @@ FA_API int fa_tile_schedule_masked(int N, const fa_mask* mask, int b, int32_t* r
                                    int32_t* col_idx, uint8_t* partial, void* stream);
 
 /*
+ * Packed variable-length sequences (page "FlashAttention" (aiwiki), section
+ * "Software integration and limitations": variable-length sequences are
+ * among the method's interfaces).  The B sequences lie back to back along
+ * the token axis:
+ *   q, k, v, o, dout, dq, dk, dv : bf16 [total, H, d] (token-major), 16-byte
+ *                                  aligned;
+ *   lse                          : fp32 [H, total];
+ *   cu_seqlens                   : int32 [B+1] device; sequence b is tokens
+ *                                  cu_seqlens[b] .. cu_seqlens[b+1]-1,
+ *                                  normally cu_seqlens[0] = 0 and
+ *                                  cu_seqlens[B] = total;
+ *   max_seqlen                   : at least every sequence's length (sizes
+ *                                  the grid; <= 8,388,480).
+ * Each sequence attends only within itself, exactly as a batch element of
+ * its own length would under fa_forward_masked: token t = cu_seqlens[b] + i
+ * is query/key i of sequence b.  mask may give causal and the sliding
+ * window; block_mask and kv_len must be NULL (FA_ERR_UNSUPPORTED otherwise).
+ * Offsets out of order, out of [0, total] or longer than max_seqlen are
+ * clamped in the kernels, which then record FA_ERR_INVALID_ARG in the error
+ * word read by fa_last_device_status.  O, LSE, dK and dV of tokens outside
+ * every sequence are not written; their dQ is 0.
+ */
+FA_API int fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* cu_seqlens, int B, int H, int total,
+                             int max_seqlen, int d, float scale, const fa_mask* mask,
+                             void* stream);
+
+/* Workspace of fa_backward_varlen: LSE*log2(e) and D per sequence row, padded
+ * (fp32 [B*H][ceil(max_seqlen/128)*128] each), then the fp32 dQ accumulator
+ * [total, H, d]; each part 256-byte aligned.  0 for invalid sizes. */
+FA_API size_t fa_varlen_workspace_bytes(int B, int H, int total, int max_seqlen, int d);
+
+/* Backward of fa_forward_varlen (same sequences, mask and scale); launches
+ * the packed preprocess, the dK/dV/dQ kernel and the dQ conversion. */
+FA_API int fa_backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              const int32_t* cu_seqlens, int B, int H, int total,
+                              int max_seqlen, int d, float scale, const fa_mask* mask,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Reads and clears the library's device error word on the current device
  * after synchronising `stream`.  Kernels that wait on an mbarrier give up
  * after a bounded number of polls, record FA_ERR_TIMEOUT there and exit,
