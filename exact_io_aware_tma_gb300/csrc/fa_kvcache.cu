@@ -60,10 +60,13 @@ constexpr int NCW = 4;                // consumer warps
 constexpr int THREADS = 32 * (1 + NCW);
 constexpr int KPW = KT / NCW;         // keys per consumer warp per stage
 constexpr int RQ_MAX = 4;             // query rows per pass
-constexpr int STAGE_BUDGET = 96 * 1024;
-
 template <int D, int RQ>
 struct Cfg {
+  // One-row passes need few registers: three CTAs per SM (more warps to hide
+  // the latency of each CTA's dependent steps), 64 KB of stages each;
+  // otherwise two CTAs with 96 KB.  Either way about 192 KB per SM in flight.
+  static constexpr int CTAS = RQ == 1 ? 3 : 2;
+  static constexpr int STAGE_BUDGET = CTAS == 3 ? 64 * 1024 : 96 * 1024;
   static constexpr int NB = D / 64;              // 64-column boxes per row
   static constexpr int BOX = KT * 128;           // one box: 64 rows x 128 B
   static constexpr int TILE = NB * BOX;          // K or V of one stage
@@ -161,7 +164,7 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
 }
 
 template <int D, int RQ>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, Cfg<D, RQ>::CTAS)
     kvcache_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, Params p) {
   using C = Cfg<D, RQ>;
@@ -416,30 +419,35 @@ __global__ void __launch_bounds__(THREADS, 2)
           }
         }
       }
-      // Online softmax over the warp's 16 keys; s becomes p in place.
+      // Online softmax over the warp's 16 keys; s becomes p in place.  The
+      // reference m moves lazily, as in the forward kernel: only when some
+      // score exceeds it by more than 8 (log2 units) is the warp max taken
+      // and u, l rescaled; otherwise p = 2^(s - m) <= 2^8 with the old m,
+      // which leaves u / l unchanged.  A row that has seen no allowed key
+      // keeps m = -inf and gets p = 0; exp2(-inf - (-inf)) is never formed.
 #pragma unroll
       for (int r = 0; r < RQ; ++r) {
         float mx = fmaxf(fmaxf(s[0][r], s[1][r]), fmaxf(s[2][r], s[3][r]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mn = fmaxf(m[r], mx);
-        // exp2(-inf - (-inf)) is never formed: a row that has seen no
-        // allowed key keeps m = -inf and gets alpha = 0, p = 0.
-        const float ref = mn == -INFINITY ? 0.f : mn;
-        const float alpha = fast_exp2(m[r] - ref);
-        m[r] = mn;
+        if (__any_sync(0xffffffffu, mx > m[r] + 8.f)) {
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float alpha = fast_exp2(m[r] - mx);  // 0 while m = -inf
+          m[r] = mx;
+          l[r] *= alpha;
+#pragma unroll
+          for (int e = 0; e < C::NC / 2; ++e) {
+            u[r][e].x *= alpha;
+            u[r][e].y *= alpha;
+          }
+        }
+        const float ref = m[r] == -INFINITY ? 0.f : m[r];
         float sum = 0.f;
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
           s[pp][r] = fast_exp2(s[pp][r] - ref);
           sum += s[pp][r];
         }
-        l[r] = fmaf(l[r], alpha, sum);
-#pragma unroll
-        for (int e = 0; e < C::NC / 2; ++e) {
-          u[r][e].x *= alpha;
-          u[r][e].y *= alpha;
-        }
+        l[r] += sum;
       }
       // p of the warp's 16 keys to shared memory, one float4 of rows per key.
       __syncwarp();
@@ -703,29 +711,20 @@ int fa_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int num_sms) {
   if (num_sms <= 0) return 0;
   const int rq = rows_per_pass(Nq);
   const long long units = (long long)B * H * ((Nq + rq - 1) / rq);
-  const long long slots = 2LL * num_sms;  // resident CTAs (two per SM)
+  const long long slots = (long long)(rq == 1 ? 3 : 2) * num_sms;  // resident CTAs
   // At most one split per 4 key tiles (256 keys), at most FA_KVCACHE_MAX_SPLITS.
   long long s_hi = ((long long)Nk + 4 * KT - 1) / (4 * KT);
   if (s_hi > FA_KVCACHE_MAX_SPLITS) s_hi = FA_KVCACHE_MAX_SPLITS;
   if (s_hi < 1) s_hi = 1;
-  long long s_lo = (2 * slots + units - 1) / units;  // at least two items per resident CTA
-  if (s_lo > s_hi) s_lo = s_hi;
-  if (s_lo < 1) s_lo = 1;
-  // Among S in [s_lo, min(4 s_lo, s_hi)] take the one whose items fill the
-  // last round of the persistent grid best (ties: fewer splits).
-  long long best = s_lo;
-  double best_eff = -1.0;
-  const long long top = 4 * s_lo < s_hi ? 4 * s_lo : s_hi;
-  for (long long s = s_lo; s <= top; ++s) {
-    const long long items = units * s;
-    const long long rounds = (items + slots - 1) / slots;
-    const double eff = (double)items / (double)(rounds * slots);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
-      best = s;
-    }
-  }
-  return (int)best;
+  // Items per resident CTA: about 1.5 for one-row passes (each extra split
+  // costs a partial write and a merge, and a little over one round already
+  // keeps HBM busy), 8 for multi-row passes (longer per-tile work: many
+  // smaller items balance better).  Measured on 128-384 head decode batches.
+  const long long want = rq == 1 ? (3 * slots + 1) / 2 : 8 * slots;
+  long long S = (want + units - 1) / units;
+  if (S > s_hi) S = s_hi;
+  if (S < 1) S = 1;
+  return (int)S;
 }
 
 size_t fa_kvcache_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {

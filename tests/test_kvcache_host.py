@@ -33,10 +33,16 @@ def test_split_choice_bounds(lib, B, H, Nq, Nk, d):
     assert S == lib.fa_kvcache_num_splits(B, H, Nq, Nk, d, 152)
 
 
-def test_split_choice_fills_the_persistent_grid(lib):
-    # 128 heads, one query row, 32768 keys on 152 SMs (304 resident CTAs):
-    # 19 splits give 2432 items = 8 full rounds of the grid.
-    assert lib.fa_kvcache_num_splits(8, 16, 1, 32768, 128, 152) == 19
+def test_split_choice_items_per_resident_cta(lib):
+    # one-row passes: 3 CTAs per SM, about 1.5 items per resident CTA
+    # (456 on 152 SMs): 128 heads -> ceil(684 / 128) = 6, 384 heads -> 2
+    assert lib.fa_kvcache_num_splits(8, 16, 1, 32768, 128, 152) == 6
+    assert lib.fa_kvcache_num_splits(32, 12, 1, 4096, 64, 152) == 2
+    # multi-row passes: 2 CTAs per SM, 8 items per resident CTA (304):
+    # ceil(2432 / 128) = 19
+    assert lib.fa_kvcache_num_splits(8, 16, 4, 32768, 128, 152) == 19
+    # capped at one split per 256 keys
+    assert lib.fa_kvcache_num_splits(1, 1, 1, 1000, 64, 152) == 4
     # Tiny caches are not split.
     assert lib.fa_kvcache_num_splits(1, 1, 1, 64, 64, 152) == 1
     assert lib.fa_kvcache_num_splits(1, 1, 1, 64, 96, 152) == 0
