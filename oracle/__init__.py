@@ -17,6 +17,7 @@ from .attention import (  # noqa: F401
     attention_forward_varlen,
     live_tiles,
 )
+from .philox import dropout_keep, dropout_p8, philox4x32_10  # noqa: F401
 from .kvcache import (  # noqa: F401
     attention_forward_kvcache,
     kvcache_allowed,

@@ -38,6 +38,14 @@ What it computes, and where the pages define it:
   is allowed only if its tile is nonzero (page "Fast and Memory Efficient
   Exact Attention", "Summary & Methodology Analysis": zero blocks of a
   predefined block-sparsity mask are skipped).
+* Dropout on the attention probabilities (page "FlashAttention: Fast and
+  Memory-Efficient Exact Attention with IO-Awareness", claims on the
+  backward pass: the dropout mask is not stored but regenerated from the
+  generator state in the backward).  Reading: inverted dropout of P,
+      O = ((P o Z) / (1 - p)) V,   Z_ij = keep bit of (b, h, i, j),
+  LSE unchanged; backward dV = ((P o Z)/(1-p))^T dO, dP = (dO V^T) o Z/(1-p),
+  D_i = sum_c dO_ic O_ic (still equal to sum_j P_ij dP_ij), dS = P o (dP - D).
+  Z comes from oracle/philox.py (Philox4x32-10, element mapping there).
 * Sliding-window masks and variable-length sequences (page "FlashAttention",
   aiwiki, section "Software integration and limitations": the method's
   software offers causal and sliding-window masks and variable-length
@@ -63,6 +71,8 @@ Readings where the pages are silent (each is listed in the design notes):
 """
 
 import numpy as np
+
+from .philox import dropout_keep
 
 TILE = 128  # side of one block-mask tile, in queries and in keys
 
@@ -111,13 +121,27 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
+def _dropout_factor(dropout, bh, rows, n):
+    """Z / (1 - p) for the given rows of head bh (None when no dropout).
+
+    ``dropout`` = dict(p8=, seed=, offset=, bh0=0): the global head index of
+    local head (b, h) is bh0 + b*H + h (a caller passing one sliced head
+    passes its global index as bh0).
+    """
+    if dropout is None or dropout["p8"] == 0:
+        return None
+    keep = dropout_keep(dropout["seed"], dropout["offset"], dropout["p8"], bh, rows,
+                        np.arange(n))
+    return keep / (1.0 - dropout["p8"] / 256.0)
+
+
 def _kv(kv_len, b):
     return None if kv_len is None else int(np.asarray(kv_len)[b])
 
 
 def attention_forward(q, k, v, scale, causal=False, block_mask=None,
                       kv_len=None, heads=None, row_chunk=1024, tile=TILE,
-                      window=None):
+                      window=None, dropout=None):
     """O [B,H,N,dv] and LSE [B,H,N] by the textbook two-pass definition.
 
     ``heads`` optionally restricts the work to a list of (b, h) pairs; the
@@ -135,7 +159,8 @@ def attention_forward(q, k, v, scale, causal=False, block_mask=None,
             ok = allowed_mask(N, rows, causal, block_mask, _kv(kv_len, b),
                               tile, window)
             p, lse[b, h, rows] = _softmax_rows(s, ok)
-            o[b, h, rows] = p @ v[b, h]
+            z = _dropout_factor(dropout, (dropout or {}).get("bh0", 0) + b * H + h, rows, N)
+            o[b, h, rows] = (p if z is None else p * z) @ v[b, h]
     return o, lse
 
 
@@ -153,7 +178,7 @@ def attention_forward_rows(q, k, v, scale, b, h, rows, causal=False,
 
 def attention_backward(q, k, v, do, scale, causal=False, block_mask=None,
                        kv_len=None, heads=None, row_chunk=1024, tile=TILE,
-                       window=None):
+                       window=None, dropout=None):
     """dQ, dK, dV [B,H,N,d] of L = sum(O * dO), plus O, LSE and D.
 
     P is rebuilt here from the inputs (the oracle stores nothing between
@@ -178,15 +203,19 @@ def attention_backward(q, k, v, do, scale, causal=False, block_mask=None,
             ok = allowed_mask(N, rows, causal, block_mask, _kv(kv_len, b),
                               tile, window)
             p, lse[b, h, rows] = _softmax_rows(s, ok)
-            o_r = p @ v[b, h]
+            z = _dropout_factor(dropout, (dropout or {}).get("bh0", 0) + b * H + h, rows, N)
+            pz = p if z is None else p * z
+            o_r = pz @ v[b, h]
             o[b, h, rows] = o_r
             d_r = np.sum(do[b, h, rows] * o_r, axis=1)
             dd[b, h, rows] = d_r
             dp = do[b, h, rows] @ v[b, h].T
+            if z is not None:
+                dp = dp * z
             ds = p * (dp - d_r[:, None])
             dq[b, h, rows] = scale * (ds @ k[b, h])
             dk[b, h] += scale * (ds.T @ q[b, h, rows])
-            dv[b, h] += p.T @ do[b, h, rows]
+            dv[b, h] += pz.T @ do[b, h, rows]
     return dq, dk, dv, o, lse, dd
 
 
@@ -257,6 +286,11 @@ def live_tiles(n, causal=False, block_mask=None, kv_len=None, tile=TILE,
     return out
 
 
+def _seq_dropout(dropout, b, H):
+    """Dropout of packed sequence b: its heads are global heads b*H + h."""
+    return None if dropout is None else dict(dropout, bh0=b * H)
+
+
 def _varlen_heads(x, cu_seqlens, b):
     """Rows of sequence b of a packed [T, H, d] array, as a [1, H, len, d] view."""
     lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
@@ -264,7 +298,7 @@ def _varlen_heads(x, cu_seqlens, b):
 
 
 def attention_forward_varlen(q, k, v, cu_seqlens, scale, causal=False,
-                             window=None):
+                             window=None, dropout=None):
     """O [T,H,d] and LSE [H,T] of packed variable-length sequences: every
     sequence b (rows cu_seqlens[b] .. cu_seqlens[b+1]-1) attends within
     itself by the same definition as a batch element of its own length."""
@@ -279,14 +313,15 @@ def attention_forward_varlen(q, k, v, cu_seqlens, scale, causal=False,
         ob, lb = attention_forward(_varlen_heads(q, cu_seqlens, b),
                                    _varlen_heads(k, cu_seqlens, b),
                                    _varlen_heads(v, cu_seqlens, b), scale,
-                                   causal=causal, window=window)
+                                   causal=causal, window=window,
+                                   dropout=_seq_dropout(dropout, b, H))
         o[lo:hi] = np.transpose(ob[0], (1, 0, 2))
         lse[:, lo:hi] = lb[0]
     return o, lse
 
 
 def attention_backward_varlen(q, k, v, do, cu_seqlens, scale, causal=False,
-                              window=None):
+                              window=None, dropout=None):
     """dQ, dK, dV [T,H,d], O [T,H,d] and LSE [H,T] of packed sequences, each
     sequence's gradient being that of its own attention."""
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
@@ -298,7 +333,8 @@ def attention_backward_varlen(q, k, v, do, cu_seqlens, scale, causal=False,
         if hi <= lo:
             continue
         r = attention_backward(*(_varlen_heads(x, cu_seqlens, b) for x in (q, k, v, do)),
-                               scale, causal=causal, window=window)
+                               scale, causal=causal, window=window,
+                               dropout=_seq_dropout(dropout, b, H))
         for dst, src in zip((dq, dk, dv, o), r[:4]):
             dst[lo:hi] = np.transpose(src[0], (1, 0, 2))
         lse[:, lo:hi] = r[4][0]
