@@ -604,21 +604,149 @@ def kvcache_e2e(inp, S, steps, dev, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+# ---------------------------------------------------------------- masks
+
+def window_pairs(N, causal, window):
+    """Allowed (i, j) pairs of one head under causal + window (exact count)."""
+    import numpy as np
+    i = np.arange(N)
+    wl, wr = window
+    lo = np.maximum(0, i - wl) if wl is not None and wl >= 0 else np.zeros_like(i)
+    hi = np.minimum(N - 1, i) if causal else np.full_like(i, N - 1)
+    if wr is not None and wr >= 0:
+        hi = np.minimum(hi, i + wr)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def run_gpu_masks(args, name):
+    """fwd + bwd on a sliding-window or packed variable-length workload; FLOPs
+    are 4*d per allowed (query, key) pair (fwd), 2.5x that (bwd), with the
+    causal count taken as N^2/2 per sequence as for the main workload."""
+    import numpy as np
+    import torch
+    from exact_io_aware_tma_gb300 import fa
+    from exact_io_aware_tma_gb300.workloads import (MASK_WORKLOADS, make_inputs,
+                                                    make_varlen_inputs)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = dict(MASK_WORKLOADS[name])
+    cfg["seed"] = rank_seed(cfg["seed"], rank)
+    varlen = "nseq" in cfg
+    if varlen:
+        inp = make_varlen_inputs(**cfg)
+        lens = np.diff(inp["cu_seqlens"])
+        H, d = cfg["H"], cfg["d"]
+        f_fwd = float(sum(4.0 * H * d * (n * n / 2 if cfg["causal"] else n * n) for n in lens))
+        cu = torch.from_numpy(inp["cu_seqlens"]).to(dev)
+        mx = inp["max_seqlen"]
+        kw = dict(causal=inp["causal"], scale=inp["scale"])
+    else:
+        window = cfg.pop("window", None)
+        dropout = cfg.pop("dropout", None)
+        inp = make_inputs(**cfg)
+        B, H, N, d = inp["q"].shape
+        pairs = N * N / 2 if (inp["causal"] and (window is None or window[0] < 0)) else \
+            window_pairs(N, inp["causal"], window)
+        f_fwd = 4.0 * B * H * d * pairs
+        kw = dict(causal=inp["causal"], scale=inp["scale"], window=window, dropout=dropout)
+        if window is not None:
+            cfg["window"] = window
+        if dropout is not None:
+            cfg["dropout"] = dropout
+    f_bwd = 2.5 * f_fwd
+    q, k, v, do = (inp[x].to(dev) for x in ("q", "k", "v", "do"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    if varlen:
+        lse = torch.empty((H, q.shape[0]), device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.varlen_workspace_bytes(len(lens), H, q.shape[0], mx, d),
+                         device=dev, dtype=torch.uint8)
+        fwd = lambda: fa.forward_varlen(q, k, v, cu, mx, out=o, lse=lse, **kw)
+        bwd = lambda: fa.backward_varlen(q, k, v, o, lse, do, cu, mx, workspace=ws, dq=dq, dk=dk,
+                                         dv=dv, **kw)
+    else:
+        lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.backward_workspace_bytes(B, H, N, d), device=dev, dtype=torch.uint8)
+        fwd = lambda: fa.forward(q, k, v, out=o, lse=lse, **kw)
+        bwd = lambda: fa.backward(q, k, v, o, lse, do, workspace=ws, dq=dq, dk=dk, dv=dv, **kw)
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(max(args.steps, args.warmup))]
+    for i in range(args.warmup):
+        flush.zero_()
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if fa.last_device_status(stream) != 0:
+        raise RuntimeError("device status not OK")
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev[:args.steps])
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev[:args.steps])
+    step_ms = max_over_ranks(fwd_ms + bwd_ms, dev)
+    peak, peak_kind = peaks()
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    achieved = bwd_tf if dom == "bwd" else fwd_tf
+    if rank == 0:
+        config = {"workload": name, **{k_: v_ for k_, v_ in cfg.items() if k_ != "seed"},
+                  "parallelism": f"replicas{world}", "l2": "flushed between steps (256 MB write)"}
+        if varlen:
+            config.update(total_tokens=int(q.shape[0]), max_seqlen=mx)
+        line = {
+            "metric": METRIC, "value": world * (f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "pct_of_peak": {"fwd": 100 * fwd_tf / peak, "bwd": 100 * bwd_tf / peak,
+                            "peak_tflops": peak, "peak_kind": peak_kind},
+            "roofline": {"bound": "tensor", "kernel": dom + " (whole call)", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": None},
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     from exact_io_aware_tma_gb300.workloads import (BENCH_WORKLOAD, KVCACHE_WORKLOADS,
-                                                    WORKLOADS)
+                                                    MASK_WORKLOADS, WORKLOADS)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=BENCH_WORKLOAD,
-                    choices=list(WORKLOADS) + list(KVCACHE_WORKLOADS))
+                    choices=list(WORKLOADS) + list(KVCACHE_WORKLOADS) + list(MASK_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kvcache", action="store_true",
                     help="skip the KV-cache decode figure of the default line")
     args = ap.parse_args()
+    if args.workload in MASK_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm is timed on the main workloads only"}))
+        else:
+            run_gpu_masks(args, args.workload)
+        return
     if args.workload in KVCACHE_WORKLOADS:
         if args.impl == "reference":
             run_reference_kvcache(args, args.workload)

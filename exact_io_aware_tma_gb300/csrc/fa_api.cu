@@ -233,11 +233,25 @@ static int check_sizes(int B, int H, int N, int d, float scale, const fa_mask* m
   p->status = nullptr;
   p->cu_seqlens = nullptr;
   p->total = 0;
+  p->drop_p8 = 0;
+  p->seed_lo = p->seed_hi = p->drop_offset = 0;
+  p->drop_scale = 1.f;
+  if (m != nullptr && m->dropout_p != 0.f) {
+    // dropout probability in steps of 1/256, below 1
+    if (!(m->dropout_p > 0.f && m->dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
+    int p8 = (int)std::lround((double)m->dropout_p * 256.0);
+    p8 = p8 > 255 ? 255 : p8;
+    p->drop_p8 = (uint32_t)p8;
+    p->seed_lo = (uint32_t)(m->dropout_seed & 0xffffffffull);
+    p->seed_hi = (uint32_t)(m->dropout_seed >> 32);
+    p->drop_offset = m->dropout_offset;
+    p->drop_scale = (float)(1.0 / (1.0 - p8 / 256.0));
+  }
   return FA_OK;
 }
 
 static fa_mask plain_mask(int causal, const uint8_t* block_mask, const int32_t* kv_len) {
-  fa_mask m;
+  fa_mask m = {};
   m.causal = causal;
   m.window_left = -1;
   m.window_right = -1;

@@ -64,7 +64,10 @@ struct BwdTc {
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
                        B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 32 + 1024;
+  // dropout keep bytes of a step, [64 queries][128 keys], two buffers
+  static constexpr int OFF_DROP = (OFF_MISC + 32 + 127) / 128 * 128;
+  static constexpr int DROPB = BQ * 128;
+  static constexpr int SMEM = OFF_DROP + 2 * DROPB + 1024;
   static constexpr int COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(2 * KT <= NS * STAGE, "dK/dV staging must fit in the stage ring");
@@ -92,7 +95,7 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, 
   return false;
 }
 
-template <int D, bool PACKED>
+template <int D, bool PACKED, bool DROP>
 __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -288,6 +291,23 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       const uint8_t* vb = smem + C::OFF_VEC + (i % C::NS) * 512;
       const float* l2 = reinterpret_cast<const float*>(vb);
       const float* dv = reinterpret_cast<const float*>(vb + 256);
+      // Dropout: the step's 64 x 128 keep bytes, generated by the four warps
+      // together (four generator calls per thread, each 16 keys of one
+      // query) while the tensor core computes S^T and dP^T, stored with the
+      // 16-byte chunk index XOR-swizzled by the query row; double-buffered,
+      // so one barrier per step keeps writers behind readers.
+      const uint8_t* drop_buf = smem + C::OFF_DROP + (i & 1) * C::DROPB;
+      if constexpr (DROP) {
+        const int c = r & 63, kh = (r >> 6) * 4;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int kb = kh + kk;
+          const uint4 w = dropout_bytes(p, bh, q0 + c, kt * 8 + kb);
+          *reinterpret_cast<uint4*>(const_cast<uint8_t*>(drop_buf) + c * 128 +
+                                    ((kb ^ (c & 7)) << 4)) = w;
+        }
+        named_barrier(2, 128);
+      }
       if (!(ok = mbar_wait(bar(C::B_S + bf), (i >> 1) & 1, ab))) break;
       tc_fence_after();
       uint32_t sr[64], pr[64];
@@ -323,10 +343,29 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
         const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2),
                     p3 = fast_exp2(x3);
         float e0, e1, e2, e3;
-        add2(e0, e1, __uint_as_float(pr[4 * c4]), __uint_as_float(pr[4 * c4 + 1]), -Dd.x, -Dd.y);
-        add2(e2, e3, __uint_as_float(pr[4 * c4 + 2]), __uint_as_float(pr[4 * c4 + 3]), -Dd.z, -Dd.w);
-        pk[2 * c4] = pack_bf16(p0, p1);
-        pk[2 * c4 + 1] = pack_bf16(p2, p3);
+        if constexpr (DROP) {
+          // P o Z / (1 - p) feeds dV; dP = (dO V^T) o Z / (1 - p) feeds dS
+          float z[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            const uint8_t u = drop_buf[c * 128 + (((r >> 4) ^ (c & 7)) << 4) + (r & 15)];
+            z[e] = u >= p.drop_p8 ? p.drop_scale : 0.f;
+          }
+          fma2(e0, e1, __uint_as_float(pr[4 * c4]), __uint_as_float(pr[4 * c4 + 1]), z[0], z[1],
+               -Dd.x, -Dd.y);
+          fma2(e2, e3, __uint_as_float(pr[4 * c4 + 2]), __uint_as_float(pr[4 * c4 + 3]), z[2],
+               z[3], -Dd.z, -Dd.w);
+          pk[2 * c4] = pack_bf16(p0 * z[0], p1 * z[1]);
+          pk[2 * c4 + 1] = pack_bf16(p2 * z[2], p3 * z[3]);
+        } else {
+          add2(e0, e1, __uint_as_float(pr[4 * c4]), __uint_as_float(pr[4 * c4 + 1]), -Dd.x,
+               -Dd.y);
+          add2(e2, e3, __uint_as_float(pr[4 * c4 + 2]), __uint_as_float(pr[4 * c4 + 3]), -Dd.z,
+               -Dd.w);
+          pk[2 * c4] = pack_bf16(p0, p1);
+          pk[2 * c4 + 1] = pack_bf16(p2, p3);
+        }
         dk[2 * c4] = pack_bf16(p0 * e0, p1 * e1);
         dk[2 * c4 + 1] = pack_bf16(p2 * e2, p3 * e3);
       }
@@ -451,7 +490,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   }
 }
 
-template <int D, bool PACKED>
+template <int D, bool PACKED, bool DROP>
 static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
                                    const void* dout, const float* lse2, const float* dvec,
                                    float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
@@ -472,7 +511,7 @@ static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* 
            make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) &&
            make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) && make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128);
   if (!maps) return cudaErrorInvalidValue;
-  auto kern = bwd_tc_kernel<D, PACKED>;
+  auto kern = bwd_tc_kernel<D, PACKED, DROP>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -483,16 +522,27 @@ static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* 
   return cudaGetLastError();
 }
 
+template <bool PACKED, bool DROP>
+static cudaError_t launch_bwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
+                                   const void* dout, const float* lse2, const float* dvec,
+                                   float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
+  return p.d == 64 ? launch_bwd_tc_t<64, PACKED, DROP>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
+                                                       dv, npad, st)
+                   : launch_bwd_tc_t<128, PACKED, DROP>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
+                                                        dv, npad, st);
+}
+
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
                           void* dk, void* dv, int npad, cudaStream_t st) {
-  if (p.cu_seqlens != nullptr)
-    return p.d == 64
-               ? launch_bwd_tc_t<64, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
-               : launch_bwd_tc_t<128, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st);
-  return p.d == 64
-             ? launch_bwd_tc_t<64, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
-             : launch_bwd_tc_t<128, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st);
+  const bool packed = p.cu_seqlens != nullptr, drop = p.drop_p8 != 0;
+  if (packed)
+    return drop ? launch_bwd_tc_d<true, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
+                : launch_bwd_tc_d<true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad,
+                                               st);
+  return drop ? launch_bwd_tc_d<false, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
+              : launch_bwd_tc_d<false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad,
+                                              st);
 }
 
 }  // namespace fa

@@ -30,7 +30,44 @@ struct Problem {
   // (it sizes the grid; each CTA takes its own sequence's length as N).
   const int32_t* cu_seqlens;
   int total;
+  // Dropout on P (kernels instantiated for it only): element (i, j) of head
+  // bh is kept iff byte j % 16 of Philox4x32-10(counter (j/16, i, bh,
+  // drop_offset), key (seed_lo, seed_hi)) is >= drop_p8; kept probabilities
+  // are scaled by drop_scale = 1 / (1 - drop_p8 / 256).
+  uint32_t drop_p8;
+  uint32_t seed_lo, seed_hi, drop_offset;
+  float drop_scale;
 };
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11), written from its published definition: ten
+// rounds, each multiplying counter words 0 and 2 by two odd constants and
+// crossing the products' high halves with words 1, 3 and the key, the key
+// advancing by two Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
+    const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The 16 keep bytes of keys 16*jb .. 16*jb+15 of query row i: byte t of the
+// result (word t/4, bits 8*(t%4)) is the uniform byte of key 16*jb + t.
+__device__ __forceinline__ uint4 dropout_bytes(const Problem& p, long long bh, int i, int jb) {
+  return philox4x32_10(make_uint4((uint32_t)jb, (uint32_t)i, (uint32_t)bh, p.drop_offset),
+                       p.seed_lo, p.seed_hi);
+}
+
+// Keep bits of four uniform bytes (bit t = byte t >= p8).
+__device__ __forceinline__ uint32_t keep4(uint32_t w, uint32_t p8) {
+  return ((w & 0xffu) >= p8 ? 1u : 0u) | (((w >> 8) & 0xffu) >= p8 ? 2u : 0u) |
+         (((w >> 16) & 0xffu) >= p8 ? 4u : 0u) | ((w >> 24) >= p8 ? 8u : 0u);
+}
 
 // Token span of sequence b in the packed layout.  Offsets that are out of
 // order, out of range or longer than N are clamped (the call then records

@@ -70,7 +70,7 @@ __device__ __forceinline__ int next_union_tile(const Problem& p, int q0, int q1,
   return p.T;
 }
 
-template <int D, bool PACKED>
+template <int D, bool PACKED, bool DROP>
 __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -364,6 +364,17 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          // dropout: keep bits of the chunk's 32 keys (two generator calls of
+          // 16 keys each); dropped probabilities still count in the row sum
+          uint32_t keep = 0xffffffffu;
+          if constexpr (DROP) {
+            const uint4 a = dropout_bytes(p, bh, row, kt * 8 + 2 * c);
+            const uint4 b2 = dropout_bytes(p, bh, row, kt * 8 + 2 * c + 1);
+            keep = keep4(a.x, p.drop_p8) | keep4(a.y, p.drop_p8) << 4 |
+                   keep4(a.z, p.drop_p8) << 8 | keep4(a.w, p.drop_p8) << 12 |
+                   keep4(b2.x, p.drop_p8) << 16 | keep4(b2.y, p.drop_p8) << 20 |
+                   keep4(b2.z, p.drop_p8) << 24 | keep4(b2.w, p.drop_p8) << 28;
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -372,7 +383,11 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
             const float p0 = fast_exp2(x0);
             const float p1 = fast_exp2(x1);
             add2(sa[j & 3], sb[j & 3], sa[j & 3], sb[j & 3], p0, p1);
-            pk[j] = pack_bf16(p0, p1);
+            if constexpr (DROP)
+              pk[j] = pack_bf16((keep >> (2 * j)) & 1u ? p0 : 0.f,
+                                (keep >> (2 * j + 1)) & 1u ? p1 : 0.f);
+            else
+              pk[j] = pack_bf16(p0, p1);
           }
           tmem_st16(lane_base + col_s + 16 * c, pk);
         }
@@ -401,7 +416,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       if (ok) ok = mbar_wait(bar(C::B_O + i), 0, ab);
       tc_fence_after();
       uint8_t* stage = smem + C::OFF_Q + i * C::TILE;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // O = u / l, times 1 / (1 - p) for the kept elements under dropout
+      const float inv = l > 0.f ? (DROP ? p.drop_scale : 1.f) / l : 0.f;
       const bool direct = PACKED && (qt + 1) * 128 > p.N;
       if (ok) {
 #pragma unroll
@@ -449,7 +465,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   }
 }
 
-template <int D, bool PACKED>
+template <int D, bool PACKED, bool DROP>
 static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
                                    void* o, float* lse, cudaStream_t st) {
   using C = FwdTc<D>;
@@ -465,7 +481,7 @@ static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* 
     maps = make_bf16_map_3d(&tq, q, D, p.N, bh, 128) && make_bf16_map_3d(&tk, k, D, p.N, bh, 128) &&
            make_bf16_map_3d(&tv, v, D, p.N, bh, 128) && make_bf16_map_3d(&to, o, D, p.N, bh, 128);
   if (!maps) return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D, PACKED>;
+  auto kern = fwd_tc_kernel<D, PACKED, DROP>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -475,13 +491,21 @@ static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* 
   return cudaGetLastError();
 }
 
+template <bool PACKED, bool DROP>
+static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
+                                   void* o, float* lse, cudaStream_t st) {
+  return p.d == 64 ? launch_fwd_tc_t<64, PACKED, DROP>(p, q, k, v, o, lse, st)
+                   : launch_fwd_tc_t<128, PACKED, DROP>(p, q, k, v, o, lse, st);
+}
+
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, cudaStream_t st) {
-  if (p.cu_seqlens != nullptr)
-    return p.d == 64 ? launch_fwd_tc_t<64, true>(p, q, k, v, o, lse, st)
-                     : launch_fwd_tc_t<128, true>(p, q, k, v, o, lse, st);
-  return p.d == 64 ? launch_fwd_tc_t<64, false>(p, q, k, v, o, lse, st)
-                   : launch_fwd_tc_t<128, false>(p, q, k, v, o, lse, st);
+  const bool packed = p.cu_seqlens != nullptr, drop = p.drop_p8 != 0;
+  if (packed)
+    return drop ? launch_fwd_tc_d<true, true>(p, q, k, v, o, lse, st)
+                : launch_fwd_tc_d<true, false>(p, q, k, v, o, lse, st);
+  return drop ? launch_fwd_tc_d<false, true>(p, q, k, v, o, lse, st)
+              : launch_fwd_tc_d<false, false>(p, q, k, v, o, lse, st);
 }
 
 }  // namespace fa

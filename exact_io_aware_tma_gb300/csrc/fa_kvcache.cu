@@ -566,61 +566,93 @@ __global__ void __launch_bounds__(THREADS, Cfg<D, RQ>::CTAS)
 
 // Merge of S partial results per row: o_part [S][rows][d] fp32 (normalised),
 // lse_part [S][rows] (natural log, -inf = empty part) -> o bf16 [rows][d],
-// lse fp32 [rows].  One warp per row.  The fold of the parts with the
-// online-normalisation update is evaluated in its closed form, which is the
-// same sum without the serial dependence from part to part: the lanes first
-// find the largest part LSE (M), then every part's weight 2^(LSE_s - M)
-// (lane s % 32 holds part s's weight), and the output loads of all parts are
-// independent of each other.  Empty parts are skipped, their rows unread.
+// lse fp32 [rows].  One warp per row; every lane carries the running
+// (m, l) of the row and the running u of its columns 4*lane + 128*i.  Parts
+// are taken eight at a time: all eight LSEs and output rows are loaded
+// before any arithmetic (the kernel is bound by memory latency, not
+// bandwidth), then the group is folded in with the online-normalisation
+// update -- its largest LSE as the group maximum, each part weighted by
+// 2^(LSE_s - m).  An empty part has weight 0 and is dropped by a select, so
+// whatever its output row holds never reaches the result.
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int S,
                    long long rows, int d, __nv_bfloat16* __restrict__ o,
                    float* __restrict__ lse) {
   constexpr int MAXV = 8;  // d <= 1024: up to 8 float4 per lane
+  constexpr int G = 8;     // parts per group
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int nv = d / 4;  // float4 per row
-  float m = -INFINITY;
-  for (int s = lane; s < S; s += 32)
-    m = fmaxf(m, __ldg(lse_part + (long long)s * rows + row) * kLog2e);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float m = -INFINITY, l = 0.f;
   float4 u[MAXV];
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) u[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-  if (m != -INFINITY) {
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      const int s = s0 + lane;
-      // 2^(-inf - M) = 0: an empty part gets weight 0 and is skipped below
-      const float w = s < S ? fast_exp2(__ldg(lse_part + (long long)s * rows + row) * kLog2e - m)
-                            : 0.f;
-      lsum += w;
-      const int n = min(32, S - s0);
-#pragma unroll 4
-      for (int j = 0; j < n; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, w, j);
-        if (wj == 0.f) continue;  // warp-uniform
+  for (int s0 = 0; s0 < S; s0 += G) {
+    const int n = min(G, S - s0);
+    float ls[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      ls[g] = g < n ? __ldg(lse_part + (long long)(s0 + g) * rows + row) * kLog2e : -INFINITY;
+    if (nv <= 32) {
+      // d <= 128: one float4 per lane and part -- load the whole group first
+      float4 x[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        x[g] = (g < n && lane < nv)
+                   ? __ldg(reinterpret_cast<const float4*>(
+                               o_part + ((long long)(s0 + g) * rows + row) * d) + lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      float mg = m;
+#pragma unroll
+      for (int g = 0; g < G; ++g) mg = fmaxf(mg, ls[g]);
+      if (mg == -INFINITY) continue;  // nothing folded yet and the group is empty
+      const float a = fast_exp2(m - mg);  // 0 while m = -inf
+      l *= a;
+      u[0].x *= a; u[0].y *= a; u[0].z *= a; u[0].w *= a;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float w = fast_exp2(ls[g] - mg);  // 0 for an empty part
+        l += w;
+        u[0].x += w != 0.f ? w * x[g].x : 0.f;
+        u[0].y += w != 0.f ? w * x[g].y : 0.f;
+        u[0].z += w != 0.f ? w * x[g].z : 0.f;
+        u[0].w += w != 0.f ? w * x[g].w : 0.f;
+      }
+      m = mg;
+    } else {
+      float mg = m;
+#pragma unroll
+      for (int g = 0; g < G; ++g) mg = fmaxf(mg, ls[g]);
+      if (mg == -INFINITY) continue;
+      const float a = fast_exp2(m - mg);
+      l *= a;
+#pragma unroll
+      for (int i = 0; i < MAXV; ++i) {
+        u[i].x *= a; u[i].y *= a; u[i].z *= a; u[i].w *= a;
+      }
+      for (int g = 0; g < n; ++g) {
+        const float w = fast_exp2(ls[g] - mg);
+        l += w;
+        if (w == 0.f) continue;  // warp-uniform
         const float4* src =
-            reinterpret_cast<const float4*>(o_part + ((long long)(s0 + j) * rows + row) * d);
+            reinterpret_cast<const float4*>(o_part + ((long long)(s0 + g) * rows + row) * d);
 #pragma unroll
         for (int i = 0; i < MAXV; ++i) {
           const int c = lane + 32 * i;
           if (c < nv) {
             const float4 x = __ldg(src + c);
-            u[i].x = fmaf(wj, x.x, u[i].x);
-            u[i].y = fmaf(wj, x.y, u[i].y);
-            u[i].z = fmaf(wj, x.z, u[i].z);
-            u[i].w = fmaf(wj, x.w, u[i].w);
+            u[i].x = fmaf(w, x.x, u[i].x);
+            u[i].y = fmaf(w, x.y, u[i].y);
+            u[i].z = fmaf(w, x.z, u[i].z);
+            u[i].w = fmaf(w, x.w, u[i].w);
           }
         }
       }
+      m = mg;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
   }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int c = lane + 32 * i;
@@ -630,7 +662,7 @@ __global__ void __launch_bounds__(256)
       *reinterpret_cast<uint2*>(o + row * d + 4 * c) = w;
     }
   }
-  if (lane == 0) lse[row] = lsum > 0.f ? (m + log2f(lsum)) * kLn2 : -INFINITY;
+  if (lane == 0) lse[row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host

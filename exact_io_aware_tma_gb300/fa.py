@@ -51,10 +51,12 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class Mask(ctypes.Structure):
-    """``fa_mask`` of include/fa.h: every mask option of the *_masked calls."""
+    """``fa_mask`` of include/fa.h: every mask option of the *_masked calls
+    (including dropout and its generator state)."""
     _fields_ = [("causal", ctypes.c_int), ("window_left", ctypes.c_int),
                 ("window_right", ctypes.c_int), ("block_mask", ctypes.c_void_p),
-                ("kv_len", ctypes.c_void_p)]
+                ("kv_len", ctypes.c_void_p), ("dropout_p", ctypes.c_float),
+                ("dropout_seed", ctypes.c_uint64), ("dropout_offset", ctypes.c_uint32)]
 
 
 class FAError(RuntimeError):
@@ -116,25 +118,30 @@ def _mask_args(N, block_mask, kv_len, B):
     return _ptr(block_mask), _ptr(kv_len)
 
 
-def _mask(N, causal, block_mask, kv_len, B, window):
+def _mask(N, causal, block_mask, kv_len, B, window, dropout=None):
+    """``dropout`` = (p, seed, offset) or None."""
     bm, kl = _mask_args(N, block_mask, kv_len, B)
     wl, wr = (-1, -1) if window is None else (
         -1 if window[0] is None else int(window[0]), -1 if window[1] is None else int(window[1]))
-    return Mask(int(bool(causal)), wl, wr, bm, kl)
+    dp, seed, off = (0.0, 0, 0) if dropout is None else dropout
+    return Mask(int(bool(causal)), wl, wr, bm, kl, float(dp), int(seed) & (2**64 - 1),
+                int(off) & 0xFFFFFFFF)
 
 
 def forward(q, k, v, causal=False, block_mask=None, kv_len=None, scale=None,
-            out=None, lse=None, stream=None, window=None):
+            out=None, lse=None, stream=None, window=None, dropout=None):
     """O, LSE = attention(q, k, v); see include/fa.h ``fa_forward_masked``.
     ``window`` = (left, right): key j allowed for query i only if
-    i - left <= j <= i + right (None or negative = unbounded side)."""
+    i - left <= j <= i + right (None or negative = unbounded side).
+    ``dropout`` = (p, seed, offset): dropout on P with the mask regenerated
+    from (seed, offset) -- pass the same triple to ``backward``."""
     lib = load()
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
-    m = _mask(N, causal, block_mask, kv_len, B, window)
+    m = _mask(N, causal, block_mask, kv_len, B, window, dropout)
     st = lib.fa_forward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
                                scale, ctypes.byref(m), _stream(stream))
     if st != FA_OK:
@@ -147,7 +154,8 @@ def backward_workspace_bytes(B, H, N, d):
 
 
 def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
-             scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None, window=None):
+             scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None, window=None,
+             dropout=None):
     """dQ, dK, dV of sum(O * dO); see include/fa.h ``fa_backward_masked``."""
     lib = load()
     _check_qkv(q, k, v, o, do)
@@ -159,7 +167,7 @@ def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    m = _mask(N, causal, block_mask, kv_len, B, window)
+    m = _mask(N, causal, block_mask, kv_len, B, window, dropout)
     st = lib.fa_backward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, scale,
                                 ctypes.byref(m), _ptr(workspace),
@@ -209,7 +217,7 @@ def _check_cu(cu_seqlens):
 
 
 def forward_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, window=None, scale=None,
-                   out=None, lse=None, stream=None):
+                   out=None, lse=None, stream=None, dropout=None):
     """O [total,H,d], LSE [H,total] of packed sequences; see ``fa_forward_varlen``."""
     lib = load()
     _check_packed(q, k, v)
@@ -218,7 +226,7 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, window=None, s
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((H, total), device=q.device, dtype=torch.float32) if lse is None else lse
-    m = _mask(1, causal, None, None, 0, window)
+    m = _mask(1, causal, None, None, 0, window, dropout)
     st = lib.fa_forward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
                                B, H, total, int(max_seqlen), d, scale, ctypes.byref(m),
                                _stream(stream))
@@ -232,7 +240,8 @@ def varlen_workspace_bytes(B, H, total, max_seqlen, d):
 
 
 def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, window=None,
-                    scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+                    scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None,
+                    dropout=None):
     """dQ, dK, dV [total,H,d] of packed sequences; see ``fa_backward_varlen``."""
     lib = load()
     _check_packed(q, k, v, o, do)
@@ -245,7 +254,7 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, w
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    m = _mask(1, causal, None, None, 0, window)
+    m = _mask(1, causal, None, None, 0, window, dropout)
     st = lib.fa_backward_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B, H, total,
                                 int(max_seqlen), d, scale, ctypes.byref(m), _ptr(workspace),

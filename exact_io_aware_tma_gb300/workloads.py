@@ -57,6 +57,19 @@ KVCACHE_WORKLOADS = {
 
 KVCACHE_BENCH_WORKLOAD = "decode_kvcache_b8_h16_nk32768_d128"
 
+# Masks beyond the five workloads above: a causal sliding window of 1024 keys
+# on the long-context shape, a packed batch of 16 causal sequences whose
+# lengths are drawn in [512, 8192] (numpy default_rng(seed)), and dropout
+# (p = 0.1, generator seed 2024) on the long-context shape.
+MASK_WORKLOADS = {
+    "sliding_window_causal_n8192_d128_w1024": dict(B=2, H=16, N=8192, d=128, mask="causal",
+                                                   window=(1023, 0), seed=8),
+    "varlen_packed_causal_16seq_d128": dict(nseq=16, H=16, d=128, len_lo=512, len_hi=8192,
+                                            causal=True, seed=9),
+    "dropout_causal_n8192_d128_p0.1": dict(B=2, H=16, N=8192, d=128, mask="causal",
+                                           dropout=(0.1, 2024, 0), seed=10),
+}
+
 
 def band_global_block_mask(n_tiles, band=1, global_every=16):
     """uint8 [T, T]: 1 where |i - j| <= band or j % global_every == 0."""
@@ -114,6 +127,20 @@ def make_kvcache_inputs(B, H, Nq, Nk, d, causal=False, seed=0, len_lo=None,
         cache_len = rng.integers(len_lo, len_hi + 1, size=B).astype(np.int32)
     return dict(q=q, k=k, v=v, causal=bool(causal), cache_len=cache_len,
                 scale=1.0 / math.sqrt(d))
+
+
+def make_varlen_inputs(nseq, H, d, len_lo, len_hi, causal=True, seed=0):
+    """Packed inputs: sequence lengths from ``numpy.random.default_rng(seed)
+    .integers(len_lo, len_hi + 1, nseq)``, then Q, K, V, dO [total, H, d] iid
+    N(0, 1) fp32 -> bf16 from ``torch.Generator('cpu').manual_seed(seed)``."""
+    lens = np.random.default_rng(seed).integers(len_lo, len_hi + 1, size=nseq)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    x = [torch.randn((total, H, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+         for _ in range(4)]
+    return dict(q=x[0], k=x[1], v=x[2], do=x[3], cu_seqlens=cu, max_seqlen=int(lens.max()),
+                causal=bool(causal), scale=1.0 / math.sqrt(d))
 
 
 def kvcache_workload_inputs(name):

@@ -83,7 +83,21 @@ FA_API const char* fa_status_string(int status);
  *   window_right  >= 0: j <= i + window_right; < 0: unbounded
  *   block_mask    uint8 [T, T] device or NULL (zero tiles are skipped)
  *   kv_len        int32 [B] device or NULL
- * A window side of N or more is the same as unbounded.
+ *   dropout_p     probability of dropping each element of P, in [0, 1),
+ *                 used in steps of 1/256 (p8 = round(256 p), at most 255);
+ *                 0 = no dropout.  O = ((P o Z) / (1 - p8/256)) V with Z the
+ *                 keep mask; LSE is that of P (unaffected).
+ *   dropout_seed, dropout_offset
+ *                 the generator state: Z(b, h, i, j) = [u >= p8] with u byte
+ *                 j % 16 of Philox4x32-10(counter (j/16, i, b*H + h,
+ *                 dropout_offset), key (seed mod 2^32, seed >> 32)), i, j
+ *                 positions within the head (within the sequence when
+ *                 packed).  The backward regenerates Z from the same state,
+ *                 so pass the forward's values (page "FlashAttention: Fast
+ *                 and Memory-Efficient Exact Attention with IO-Awareness",
+ *                 claims on the backward pass: the mask is not stored).
+ * A window side of N or more is the same as unbounded.  Dropout is not
+ * offered by the plain (non-_masked) calls.
  */
 typedef struct fa_mask {
   int causal;
@@ -91,6 +105,9 @@ typedef struct fa_mask {
   int window_right;
   const uint8_t* block_mask;
   const int32_t* kv_len;
+  float dropout_p;
+  uint64_t dropout_seed;
+  uint32_t dropout_offset;
 } fa_mask;
 
 /*

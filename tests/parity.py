@@ -41,8 +41,10 @@ def to_device(inp, dev="cuda"):
 
 def run_gpu(inp, backward=True):
     g = to_device(inp)
+    drop = inp.get("dropout")
     kw = dict(causal=g["causal"], block_mask=g["block_mask"], kv_len=g["kv_len"],
-              scale=g["scale"], window=inp.get("window"))
+              scale=g["scale"], window=inp.get("window"),
+              dropout=None if drop is None else (drop["p"], drop["seed"], drop["offset"]))
     o, lse = fa.forward(g["q"], g["k"], g["v"], **kw)
     res = dict(o=o, lse=lse)
     if backward:

@@ -8,7 +8,7 @@ import torch
 from exact_io_aware_tma_gb300 import fa
 from exact_io_aware_tma_gb300.workloads import (WORKLOADS, make_inputs,
                                                 workload_inputs, to_f64)
-from oracle import attention_backward, attention_forward_rows, live_tiles
+from oracle import attention_backward, attention_forward_rows, dropout_p8, live_tiles
 from parity import (TOL_GRAD, TOL_O, check_close, check_lse, compare_heads,
                     oracle_inputs, run_gpu, to_device)
 
@@ -23,8 +23,11 @@ def oracle_on_heads(inp, heads):
     for b, h in heads:
         kv = None if inp["kv_len"] is None else inp["kv_len"][b:b + 1]
         sl = (slice(b, b + 1), slice(h, h + 1))
+        drop = inp.get("dropout")
+        drop = None if drop is None else dict(p8=dropout_p8(drop["p"]), seed=drop["seed"],
+                                              offset=drop["offset"], bh0=b * H + h)
         r = attention_backward(q[sl], k[sl], v[sl], do[sl], inp["scale"], inp["causal"],
-                               inp["block_mask"], kv, window=inp.get("window"))
+                               inp["block_mask"], kv, window=inp.get("window"), dropout=drop)
         for arr, val in zip(out, (r[0], r[1], r[2], r[3], r[4])):
             arr[b, h] = val[0, 0]
     return tuple(out)
