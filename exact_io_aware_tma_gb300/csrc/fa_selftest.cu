@@ -50,11 +50,18 @@ __global__ void __launch_bounds__(128, 1)
 
   const int b_halves = (mode == 0) ? 2 : n / 64;
   if (threadIdx.x == 0) {
-    const bool a_by_tma = (mode == 0 || mode == 1 || mode == 4);
-    mbar_expect_tx(bars, (a_by_tma ? 2 * kHalf : 0) + b_halves * kHalf);
-    if (a_by_tma)
-      for (int h = 0; h < 2; ++h) tma_load_3d(sA + h * kHalf, &tm_a, bars, h * 64, 0, 0);
-    for (int h = 0; h < b_halves; ++h) tma_load_3d(sB + h * kHalf, &tm_b, bars, h * 64, 0, 0);
+    if (mode == 5) {
+      // 8-bit: one 128-byte-wide box of 128 rows per operand
+      mbar_expect_tx(bars, 2 * kHalf);
+      tma_load_3d(sA, &tm_a, bars, 0, 0, 0);
+      tma_load_3d(sB, &tm_b, bars, 0, 0, 0);
+    } else {
+      const bool a_by_tma = (mode == 0 || mode == 1 || mode == 4);
+      mbar_expect_tx(bars, (a_by_tma ? 2 * kHalf : 0) + b_halves * kHalf);
+      if (a_by_tma)
+        for (int h = 0; h < 2; ++h) tma_load_3d(sA + h * kHalf, &tm_a, bars, h * 64, 0, 0);
+      for (int h = 0; h < b_halves; ++h) tma_load_3d(sB + h * kHalf, &tm_b, bars, h * 64, 0, 0);
+    }
   }
   if (mode == 2) {
     // A row r -> TMEM lane r, columns 128..191 (two bf16 per 32-bit column)
@@ -82,7 +89,14 @@ __global__ void __launch_bounds__(128, 1)
   bool ok = mbar_wait(bars, 0, ab);
   if (ok && threadIdx.x == 0) {
     tc_fence_after();
-    if (mode == 4) {
+    if (mode == 5) {
+      // c = a b^T with e4m3 operands, both K-major: K = 128 in four steps of
+      // 32 elements (32 bytes) along the swizzled rows
+      const uint32_t id = idesc_e4m3(128, 128);
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss_f8(tmem, sdesc_sw128(sA + kk * 32, 16, 1024), sdesc_sw128(sB + kk * 32, 16, 1024),
+                  id, kk > 0);
+    } else if (mode == 4) {
       // c = a^T b: A operand MN-major (M = columns of a, K = rows of a)
       const uint32_t id = idesc_bf16(128, n, true, true);
       for (int kk = 0; kk < 8; ++kk)
@@ -112,7 +126,7 @@ __global__ void __launch_bounds__(128, 1)
   ok = ok && mbar_wait(bars + 8, 0, ab);
   tc_fence_after();
   if (ok) {
-    const int ncols = (mode == 0) ? 128 : n;
+    const int ncols = (mode == 0 || mode == 5) ? 128 : n;
     for (int c0 = 0; c0 < ncols; c0 += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
@@ -130,11 +144,16 @@ using namespace fa;
 
 extern "C" int fa_selftest_mma(int mode, const void* a, const void* b, float* c, int n,
                                void* stream) {
-  if (mode < 0 || mode > 4 || !a || !b || !c) return 1;
-  if (mode != 0 && n != 64 && n != 128) return 1;
+  if (mode < 0 || mode > 5 || !a || !b || !c) return 1;
+  if (mode != 0 && mode != 5 && n != 64 && n != 128) return 1;
   CUtensorMap ta, tb;
-  if (!make_bf16_map_3d(&ta, a, 128, 128, 1, 128)) return 3;
-  if (!make_bf16_map_3d(&tb, b, mode == 0 ? 128 : n, 128, 1, 128)) return 3;
+  if (mode == 5) {
+    if (!make_u8_map_3d(&ta, a, 128, 128, 1, 128) || !make_u8_map_3d(&tb, b, 128, 128, 1, 128))
+      return 3;
+  } else {
+    if (!make_bf16_map_3d(&ta, a, 128, 128, 1, 128)) return 3;
+    if (!make_bf16_map_3d(&tb, b, mode == 0 ? 128 : n, 128, 1, 128)) return 3;
+  }
   const int smem = 4 * kHalf + 1024 + 256;
   if (cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)

@@ -41,6 +41,23 @@ inline bool make_bf16_map_3d(CUtensorMap* m, const void* base, int cols, int row
   return r == CUDA_SUCCESS;
 }
 
+// 8-bit tensor viewed as [heads][rows][cols] (cols contiguous, a multiple of
+// 16), copied in boxes of 128 columns (128 bytes) x box_rows rows with the
+// 128-byte swizzle; rows past `rows` read as zero.
+inline bool make_u8_map_3d(CUtensorMap* m, const void* base, int cols, int rows,
+                           long long heads, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)cols * (cuuint64_t)rows};
+  cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // bf16 tensor in the packed token-major layout [tokens][heads][cols], viewed
 // as (cols, heads, tokens) so that a box of 64 columns x 1 head x box_rows
 // tokens lands in shared memory exactly like a box of the layout above

@@ -21,6 +21,8 @@
  *   mode 4: c = a^T * b (a MN-major via TMA, i.e. the M index runs along
  *           a's rows in memory; b MN-major via TMA; the dQ^T = K^T dS^T
  *           path of the backward).
+ *   mode 5: c = a * b^T with a, b e4m3 (8-bit float) [128][128] row-major,
+ *           both K-major via TMA (the FP8 S = Q K^T and O += P V paths).
  *   n    : 64 or 128 (modes 1-4).
  * Returns 0 on success, 1 on a bad argument, 3 on a CUDA error.  A bounded
  * wait that gives up is reported by fa_last_device_status().

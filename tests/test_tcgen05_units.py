@@ -28,3 +28,17 @@ def test_single_tile_mma(mode, n):
     err = (c.double() - ref).abs().max().item()
     # fp32 accumulation of 128 exact bf16 products
     assert err <= 1e-5 * ref.abs().max().item() * 16, (mode, n, err)
+
+
+def test_single_tile_mma_e4m3():
+    # mode 5: both operands e4m3, c = a b^T; products of two e4m3 values are
+    # exact in fp32, so only the fp32 accumulation order differs
+    g = torch.Generator().manual_seed(555)
+    a = (4 * torch.randn(128, 128, generator=g)).to(torch.float8_e4m3fn)
+    b = (4 * torch.randn(128, 128, generator=g)).to(torch.float8_e4m3fn)
+    c = fa.selftest_mma(5, a.view(torch.uint8).cuda(), b.view(torch.uint8).cuda(), 128)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    ref = a.to(torch.float64) @ b.to(torch.float64).T
+    err = (c.double().cpu() - ref).abs().max().item()
+    assert err <= 1e-5 * ref.abs().max().item() * 16, err
