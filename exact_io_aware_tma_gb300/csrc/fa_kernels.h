@@ -16,4 +16,10 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
                           void* dk, void* dv, int npad, cudaStream_t st);
 
+// e4m3 forward (d = 128) on quantised operands: q8, k8 [B*H][N][128],
+// vt8 [B*H][128][ceil(N/128)*128], q/k scales [B*H][T], v scale [B*H].
+cudaError_t launch_fwd_fp8(const Problem& p, const void* q8, const void* k8, const void* vt8,
+                           const float* q_scale, const float* k_scale, const float* v_scale,
+                           void* o, float* lse, cudaStream_t st);
+
 }  // namespace fa

@@ -1,5 +1,5 @@
-"""ctypes binding of ``libfa_gb300.so`` (C ABI declared in include/fa.h and
-include/fa_kvcache.h).
+"""ctypes binding of ``libfa_gb300.so`` (C ABI declared in include/fa.h,
+include/fa_kvcache.h and include/fa_fp8.h).
 
 Argument marshalling only: every step of attention runs in the library's
 CUDA kernels.  PyTorch provides device memory and the current stream.  If the
@@ -38,6 +38,10 @@ SIGNATURES = {
     "fa_forward_varlen": ([_vp] * 6 + [_i] * 5 + [_f, _vp, _vp], _i),
     "fa_varlen_workspace_bytes": ([_i] * 5, _sz),
     "fa_backward_varlen": ([_vp] * 10 + [_i] * 5 + [_f, _vp, _vp, _sz, _vp], _i),
+    "fa_fp8_workspace_bytes": ([_i] * 4, _sz),
+    "fa_fp8_quantize": ([_vp] * 3 + [_i] * 4 + [_vp, _sz, _vp], _i),
+    "fa_forward_fp8_quantized": ([_vp, _vp, _vp] + [_i] * 4 + [_f, _i, _vp], _i),
+    "fa_forward_fp8": ([_vp] * 5 + [_i] * 4 + [_f, _i, _vp, _sz, _vp], _i),
     "fa_kvcache_num_splits": ([_i] * 6, _i),
     "fa_kvcache_workspace_bytes": ([_i] * 6, _sz),
     "fa_forward_kvcache": ([_vp] * 5 + [_i] * 5 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
@@ -262,6 +266,72 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, w
     if st != FA_OK:
         raise FAError(st, "fa_backward_varlen")
     return dq, dk, dv
+
+
+def fp8_workspace_bytes(B, H, N, d):
+    return int(load().fa_fp8_workspace_bytes(B, H, N, d))
+
+
+def fp8_workspace_views(ws, B, H, N):
+    """Views of the parts of an FP8 workspace (layout in include/fa_fp8.h):
+    q8, k8 uint8 [B*H, N, 128], vt8 uint8 [B*H, 128, Np], q/k scales fp32
+    [B*H, T], v scales fp32 [B*H]."""
+    T = (N + 127) // 128
+    bh = B * H
+
+    def r256(x):
+        return -(-x // 256) * 256
+    sizes = [bh * N * 128, bh * N * 128, bh * 128 * T * 128, bh * T * 4, bh * T * 4, bh * 4]
+    offs = [0]
+    for sz in sizes:
+        offs.append(offs[-1] + r256(sz))
+    u8 = ws.view(torch.uint8)
+    q8 = u8[offs[0]:offs[0] + sizes[0]].view(bh, N, 128)
+    k8 = u8[offs[1]:offs[1] + sizes[1]].view(bh, N, 128)
+    vt8 = u8[offs[2]:offs[2] + sizes[2]].view(bh, 128, T * 128)
+    qs = u8[offs[3]:offs[3] + sizes[3]].view(torch.float32).view(bh, T)
+    ks = u8[offs[4]:offs[4] + sizes[4]].view(torch.float32).view(bh, T)
+    vs = u8[offs[5]:offs[5] + sizes[5]].view(torch.float32)
+    return dict(q8=q8, k8=k8, vt8=vt8, qs=qs, ks=ks, vs=vs)
+
+
+def fp8_quantize(q, k, v, workspace=None, stream=None):
+    """Block-quantise bf16 q, k, v [B,H,N,128] to e4m3 into a workspace
+    (``fa_fp8_quantize``); returns the workspace."""
+    lib = load()
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    nbytes = fp8_workspace_bytes(B, H, N, d)
+    if nbytes == 0:
+        raise FAError(FA_ERR_UNSUPPORTED if d != 128 else FA_ERR_INVALID_ARG, "fa_fp8_quantize")
+    if workspace is None:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    st = lib.fa_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fp8_quantize")
+    return workspace
+
+
+def forward_fp8(q, k, v, causal=False, scale=None, workspace=None, out=None, lse=None,
+                stream=None):
+    """O, LSE of the FP8 forward with block quantisation (include/fa_fp8.h);
+    q, k, v bf16 [B,H,N,128]."""
+    lib = load()
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = fp8_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    st = lib.fa_forward_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, scale,
+                            int(bool(causal)), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_forward_fp8")
+    return out, lse
 
 
 def kvcache_num_splits(B, H, Nq, Nk, d, num_sms=0):
