@@ -637,6 +637,8 @@ def run_gpu_masks(args, name):
     dev = torch.device("cuda", local)
     cfg = dict(MASK_WORKLOADS[name])
     cfg["seed"] = rank_seed(cfg["seed"], rank)
+    if cfg.pop("fp8", False):
+        return run_gpu_fp8(args, name, cfg, dev, rank, world, local)
     varlen = "nseq" in cfg
     if varlen:
         inp = make_varlen_inputs(**cfg)
@@ -723,6 +725,78 @@ def run_gpu_masks(args, name):
             "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
+
+
+def run_gpu_fp8(args, name, cfg, dev, rank, world, local):
+    """FP8 forward (block quantisation + e4m3 attention kernel): forward FLOPs
+    over the time of the two; the attention kernel's roofline against the
+    e4m3 tensor peak (the measured bf16 peak times the nominal fp8/bf16
+    ratio 4.5 / 2.25)."""
+    import torch
+    from exact_io_aware_tma_gb300 import fa
+    from exact_io_aware_tma_gb300.workloads import make_inputs
+    inp = make_inputs(**cfg, with_grad=False)
+    B, H, N, d = inp["q"].shape
+    f_fwd = 4.0 * B * H * N * N * d * (0.5 if inp["causal"] else 1.0)
+    q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    ws = torch.empty(fa.fp8_workspace_bytes(B, H, N, d), device=dev, dtype=torch.uint8)
+    lib = fa.load()
+    stream = torch.cuda.current_stream(dev)
+    sp = fa._stream(stream)
+    P = fa._ptr
+    wsb = ws.numel()
+
+    def step(evs=None):
+        s1 = lib.fa_fp8_quantize(P(q), P(k), P(v), B, H, N, d, P(ws), wsb, sp)
+        if evs:
+            evs[1].record(stream)
+        s2 = lib.fa_forward_fp8_quantized(P(ws), P(o), P(lse), B, H, N, d, inp["scale"],
+                                          int(inp["causal"]), sp)
+        if s1 or s2:
+            raise RuntimeError("fp8 call failed")
+
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            step(e)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+    if fa.last_device_status(stream) != 0:
+        raise RuntimeError("device status not OK")
+    quant_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = max_over_ranks(quant_ms + attn_ms, dev)
+    bf16_peak, kind = peaks()
+    peak = bf16_peak * (4.5 / 2.25)
+    attn_tf = f_fwd / (attn_ms * 1e-3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "FP8 attention forward TFLOP/s (e4m3 operands, block-quantised)",
+            "value": world * f_fwd / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": name, "B": B, "H": H, "N": N, "d": d, "mask": cfg["mask"],
+                       "parallelism": f"replicas{world}",
+                       "l2": "flushed between steps (256 MB write)"},
+            "kernel_ms": {"quantise": quant_ms, "attention": attn_ms},
+            "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": attn_tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": attn_tf / peak,
+                         "peak_kind": kind + " bf16 x 2 (nominal e4m3/bf16 ratio)",
+                         "traffic": None},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": 5 * args.steps,
+            "clocks": clk.summary(),
+        }), flush=True)
 
 
 def main():

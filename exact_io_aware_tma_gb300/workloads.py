@@ -59,8 +59,9 @@ KVCACHE_BENCH_WORKLOAD = "decode_kvcache_b8_h16_nk32768_d128"
 
 # Masks beyond the five workloads above: a causal sliding window of 1024 keys
 # on the long-context shape, a packed batch of 16 causal sequences whose
-# lengths are drawn in [512, 8192] (numpy default_rng(seed)), and dropout
-# (p = 0.1, generator seed 2024) on the long-context shape.
+# lengths are drawn in [512, 8192] (numpy default_rng(seed)), dropout
+# (p = 0.1, generator seed 2024) on the long-context shape, and the FP8
+# forward on the long-context shape.
 MASK_WORKLOADS = {
     "sliding_window_causal_n8192_d128_w1024": dict(B=2, H=16, N=8192, d=128, mask="causal",
                                                    window=(1023, 0), seed=8),
@@ -68,6 +69,8 @@ MASK_WORKLOADS = {
                                             causal=True, seed=9),
     "dropout_causal_n8192_d128_p0.1": dict(B=2, H=16, N=8192, d=128, mask="causal",
                                            dropout=(0.1, 2024, 0), seed=10),
+    "fp8_forward_causal_n8192_d128": dict(B=2, H=16, N=8192, d=128, mask="causal", fp8=True,
+                                          seed=11),
 }
 
 
