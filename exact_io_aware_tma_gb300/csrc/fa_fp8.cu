@@ -109,13 +109,15 @@ __global__ void __launch_bounds__(256)
 }
 
 // V codes, transposed: one CTA per 128-key block of one (b, h) reads the
-// [128 keys][128] bf16 block, scales by the head's scale (max over the
-// head's block maxima) and writes [128][128 keys] e4m3 into Vt [BH][128][Np]
-// (keys past N as zero codes) through a shared-memory transpose.
+// [128 keys][128] bf16 block in 16-byte chunks (8 values of one key),
+// scales by the head's scale (max over the head's block maxima), writes the
+// codes transposed into a padded shared tile, and stores [128][128 keys]
+// e4m3 rows of Vt [BH][128][Np] in 16-byte chunks (keys past N as zero codes).
 __global__ void __launch_bounds__(256)
     quant_vt_kernel(const __nv_bfloat16* __restrict__ v, const float* __restrict__ amax,
                     uint8_t* __restrict__ vt, float* __restrict__ vscale, int N, int T, int Np) {
-  __shared__ uint8_t tile[128][129];
+  constexpr int LD = 128 + 16;  // row pitch of the transposed tile (bytes)
+  __shared__ __align__(16) uint8_t tile[128 * LD];
   __shared__ float red[8];
   const long long bh = blockIdx.x;
   const int t = blockIdx.y;
@@ -125,19 +127,27 @@ __global__ void __launch_bounds__(256)
   const float s = m > 0.f ? __fdiv_rn(m, kE4m3Max) : 1.f;
   if (t == 0 && threadIdx.x == 0) vscale[bh] = s;
   const int rows = min(128, N - t * 128);
-  for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
-    const int key = i >> 7, col = i & 127;
-    uint8_t c = 0;
-    if (key < rows) {
-      const float f = __bfloat162float(v[(bh * N + (long long)t * 128 + key) * 128 + col]);
-      c = to_e4m3(__fdiv_rn(f, s));
+  const __nv_bfloat16* src = v + (bh * N + (long long)t * 128) * 128;
+  // 2048 chunks: chunk c = key (c / 16), columns 8 * (c % 16) .. +7
+  for (int c = threadIdx.x; c < 2048; c += blockDim.x) {
+    const int key = c >> 4, col0 = (c & 15) * 8;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (key < rows) w = *reinterpret_cast<const uint4*>(src + key * 128 + col0);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      tile[(col0 + 2 * e) * LD + key] = key < rows ? to_e4m3(__fdiv_rn(f.x, s)) : 0;
+      tile[(col0 + 2 * e + 1) * LD + key] = key < rows ? to_e4m3(__fdiv_rn(f.y, s)) : 0;
     }
-    tile[col][key] = c;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
-    const int col = i >> 7, key = i & 127;
-    vt[(bh * 128 + col) * (long long)Np + (long long)t * 128 + key] = tile[col][key];
+  // 1024 chunks of 16 codes: chunk c = column (c / 8), keys 16 * (c % 8) .. +15
+  uint8_t* dst = vt + bh * 128 * (long long)Np + (long long)t * 128;
+  for (int c = threadIdx.x; c < 1024; c += blockDim.x) {
+    const int col = c >> 3, k0 = (c & 7) * 16;
+    *reinterpret_cast<uint4*>(dst + (long long)col * Np + k0) =
+        *reinterpret_cast<const uint4*>(&tile[col * LD + k0]);
   }
 }
 
