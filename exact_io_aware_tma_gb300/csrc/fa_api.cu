@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256)
 // The same preprocess for the packed variable-length layout: row `row` of
 // (b, h) is token cu_seqlens[b] + row of [total][H][d] (rows at or past the
 // sequence's length are padding); LSE is [H][total].  The fp32 dQ
-// accumulator [total][H][d] is cleared in full, so tokens outside every
+// accumulator [H][total][d] is cleared in full, so tokens outside every
 // sequence end with dQ = 0.
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -124,6 +124,32 @@ __global__ void __launch_bounds__(256)
   const long long nz = (long long)total * H * D / 4;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nz; i += stride)
     reinterpret_cast<float4*>(dq_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Packed layout: dQ [total][H][d] = scale * dQacc [H][total][d], fp32 ->
+// bf16, 8 elements per thread (consecutive threads: consecutive chunks of
+// one token's heads, so the bf16 writes are contiguous).
+__global__ void __launch_bounds__(256)
+    dq_convert_packed_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                             float scale, int H, int total, int d) {
+  const long long chunks = (long long)total * H * (d / 8);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long e = i * 8;  // element of dq [total][H][d]
+    const int c = (int)(e % d);
+    const long long th = e / d;
+    const int h = (int)(th % H);
+    const long long t = th / H;
+    const float* src = dq_acc + ((long long)h * total + t) * d + c;
+    const float4 a = reinterpret_cast<const float4*>(src)[0];
+    const float4 b = reinterpret_cast<const float4*>(src)[1];
+    uint4 r;
+    r.x = pack_bf16(a.x * scale, a.y * scale);
+    r.y = pack_bf16(a.z * scale, a.w * scale);
+    r.z = pack_bf16(b.x * scale, b.y * scale);
+    r.w = pack_bf16(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + e) = r;
+  }
 }
 
 // dQ = scale * dQacc, fp32 -> bf16, 8 elements per thread.
@@ -213,7 +239,8 @@ static int check_sizes(int B, int H, int N, int d, float scale, const fa_mask* m
   const long long bh = (long long)B * H;
   if (bh > 2147483647LL) return FA_ERR_INVALID_ARG;
   const long long T = ((long long)N + kTile - 1) / kTile;
-  if (T > 65535) return FA_ERR_INVALID_ARG;  // grid.y bound: N <= 8,388,480
+  if (T > 65535) return FA_ERR_INVALID_ARG;  // N <= 8,388,480
+  if (bh * T > 2147483647LL) return FA_ERR_INVALID_ARG;  // one CTA per (head, tile)
   // B*H*N*d elements must stay far from int64 overflow
   if ((double)bh * N * d > 4.0e18) return FA_ERR_INVALID_ARG;
   p->B = B;
@@ -544,8 +571,8 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
   cudaError_t e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   const long long chunks = (long long)total * H * (d / 8);
-  dq_convert_kernel<<<elementwise_blocks(chunks), 256, 0, s>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), scale, chunks);
+  dq_convert_packed_kernel<<<elementwise_blocks(chunks), 256, 0, s>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), scale, H, total, d);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

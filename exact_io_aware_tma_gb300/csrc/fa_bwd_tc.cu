@@ -107,8 +107,12 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
   // (coordinates (x, h, start + row)), whose length then plays the role of N.
-  const long long bh = blockIdx.x;
-  const int kt = blockIdx.y;  // small key tiles carry the most causal work: first
+  // Grid: one CTA per (head, key tile) in the grouped order -- small key
+  // tiles carry the most causal work: first, across a group of heads whose
+  // Q, dO and dQ accumulator stay in L2.
+  long long bh;
+  int kt;
+  grouped_cta(pin, blockIdx.x, pin.T, bh, kt);
   const int b = (int)(bh / pin.H);
   const int head = (int)(bh % pin.H);
   Problem p = pin;
@@ -472,9 +476,11 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       // query the warp's 32 lanes add 32 consecutive floats of its row.
       if (valid) {
         const int rows = min(64, p.N - q0);
-        // padded: [B*H][N][d]; packed: [total][H][d]
-        const size_t row_stride = PACKED ? (size_t)p.H * D : (size_t)D;
-        float* dst = PACKED ? dq_acc + ((size_t)(start + q0) * p.H + head) * D + c
+        // padded: [B*H][N][d]; packed: [H][total][d] (head-major, so a head's
+        // rows are contiguous and the reductions do not collide in L2 the way
+        // rows H*d apart do)
+        const size_t row_stride = (size_t)D;
+        float* dst = PACKED ? dq_acc + ((size_t)head * p.total + start + q0) * D + c
                             : dq_acc + ((size_t)bh * p.N + q0) * D + c;
 #pragma unroll
         for (int q = 0; q < 64; ++q)
@@ -491,10 +497,19 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
 }
 
 template <int D, bool PACKED, bool DROP>
-static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
-                                   const void* dout, const float* lse2, const float* dvec,
-                                   float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
+static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void* k,
+                                   const void* v, const void* dout, const float* lse2,
+                                   const float* dvec, float* dq_acc, void* dk, void* dv, int npad,
+                                   cudaStream_t st) {
   using C = BwdTc<D>;
+  // Heads per CTA group: Q, dO (bf16) and the fp32 dQ accumulator of a group
+  // within about 64 MB (half of L2).
+  Problem p = pin;
+  {
+    const long long heads = (long long)p.B * p.H;
+    long long g = (64ll << 20) / ((long long)p.N * D * 8);
+    p.hgroup = (int)(g < 1 ? 1 : (g > heads ? heads : g));
+  }
   const long long bh = (long long)p.B * p.H;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   bool maps;
@@ -515,7 +530,7 @@ static cudaError_t launch_bwd_tc_t(const Problem& p, const void* q, const void* 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)bh, (unsigned)p.T);
+  dim3 grid((unsigned)(bh * p.T));
   kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad,
                                           static_cast<__nv_bfloat16*>(dk),
                                           static_cast<__nv_bfloat16*>(dv));

@@ -30,6 +30,10 @@ struct Problem {
   // (it sizes the grid; each CTA takes its own sequence's length as N).
   const int32_t* cu_seqlens;
   int total;
+  // CTA order: heads go in groups of hgroup (sized by the host so that a
+  // group's working set fits in about half of L2); within a group the CTAs
+  // walk the tiles heaviest first, cycling over the group's heads.
+  int hgroup;
   // Dropout on P (kernels instantiated for it only): element (i, j) of head
   // bh is kept iff byte j % 16 of Philox4x32-10(counter (j/16, i, bh,
   // drop_offset), key (seed_lo, seed_hi)) is >= drop_p8; kept probabilities
@@ -67,6 +71,20 @@ __device__ __forceinline__ uint4 dropout_bytes(const Problem& p, long long bh, i
 __device__ __forceinline__ uint32_t keep4(uint32_t w, uint32_t p8) {
   return ((w & 0xffu) >= p8 ? 1u : 0u) | (((w >> 8) & 0xffu) >= p8 ? 2u : 0u) |
          (((w >> 16) & 0xffu) >= p8 ? 4u : 0u) | ((w >> 24) >= p8 ? 8u : 0u);
+}
+
+// Head and tile rank of CTA `cta` of a grid of B*H x ntiles CTAs in the
+// grouped order above (the last group may hold fewer heads).
+__device__ __forceinline__ void grouped_cta(const Problem& p, long long cta, int ntiles,
+                                            long long& bh, int& rank) {
+  const long long heads = (long long)p.B * p.H;
+  const long long per_group = (long long)p.hgroup * ntiles;
+  const long long g = cta / per_group;
+  const long long j = cta - g * per_group;
+  const long long first = g * p.hgroup;
+  const int gsize = (int)min((long long)p.hgroup, heads - first);
+  rank = (int)(j / gsize);
+  bh = first + j % gsize;
 }
 
 // Token span of sequence b in the packed layout.  Offsets that are out of

@@ -191,6 +191,7 @@ static int check(int B, int H, int N, int d, float scale) {
   const long long bh = (long long)B * H;
   if (bh > 2147483647LL) return FA_ERR_INVALID_ARG;
   if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARG;  // grid.y: 128-row blocks
+  if (bh * ((N + 127) / 128) > 2147483647LL) return FA_ERR_INVALID_ARG;
   if ((double)bh * N * d > 4.0e18) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }

@@ -77,9 +77,13 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   const Abort ab{abort_flag, p.status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Grid: grouped order (heaviest pairs first across a group of heads whose
+  // K and V stay in L2).
   const int npairs = (p.T + 1) / 2;
-  const int pair = npairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
-  const long long bh = blockIdx.x;
+  long long bh;
+  int yi;
+  grouped_cta(p, blockIdx.x, npairs, bh, yi);
+  const int pair = npairs - 1 - yi;
   const int qt0 = 2 * pair;
   const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
   const int klim = p.N;
@@ -388,10 +392,17 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   }
 }
 
-cudaError_t launch_fwd_fp8(const Problem& p, const void* q8, const void* k8, const void* vt8,
+cudaError_t launch_fwd_fp8(const Problem& pin, const void* q8, const void* k8, const void* vt8,
                            const float* q_scale, const float* k_scale, const float* v_scale,
                            void* o, float* lse, cudaStream_t st) {
   using C = Fp8Cfg;
+  // Heads per CTA group: e4m3 K and V of a group within about 64 MB.
+  Problem p = pin;
+  {
+    const long long heads = (long long)p.B * p.H;
+    long long g = (64ll << 20) / ((long long)p.N * 128 * 2);
+    p.hgroup = (int)(g < 1 ? 1 : (g > heads ? heads : g));
+  }
   const long long bh = (long long)p.B * p.H;
   CUtensorMap tq, tk, tvt, to;
   if (!make_u8_map_3d(&tq, q8, 128, p.N, bh, 128) || !make_u8_map_3d(&tk, k8, 128, p.N, bh, 128) ||
@@ -401,7 +412,7 @@ cudaError_t launch_fwd_fp8(const Problem& p, const void* q8, const void* k8, con
   cudaError_t e =
       cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)bh, (unsigned)((p.T + 1) / 2));
+  dim3 grid((unsigned)(bh * ((p.T + 1) / 2)));
   fwd_fp8_kernel<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tvt, to, p, q_scale, k_scale, v_scale,
                                                     lse);
   return cudaGetLastError();

@@ -79,7 +79,12 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
   // (coordinates (x, h, start + row)), whose length then plays the role of N.
-  const long long bh = blockIdx.x;
+  // Grid: one CTA per (head, query-tile pair) in the grouped order
+  // (heaviest pairs first across a group of heads whose K and V stay in L2).
+  const int npairs_grid = (pin.T + 1) / 2;
+  long long bh;
+  int yi;
+  grouped_cta(pin, blockIdx.x, npairs_grid, bh, yi);
   const int b = (int)(bh / pin.H);
   const int head = (int)(bh % pin.H);
   Problem p = pin;
@@ -91,7 +96,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     p.T = (len + kTile - 1) / kTile;
   }
   const int npairs = (p.T + 1) / 2;
-  if ((int)blockIdx.y >= npairs) return;  // packed: past this sequence's tiles
+  if (yi >= npairs) return;  // packed: past this sequence's tiles
   auto cy = [&](int row) { return PACKED ? head : row; };
   auto cz = [&](int row) { return PACKED ? start + row : (int)bh; };
   extern __shared__ uint8_t smem_raw[];
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   const Abort ab{abort_flag, p.status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = npairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
+  const int pair = npairs - 1 - yi;  // heaviest causal pairs first
   const int qt0 = 2 * pair;
   const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
   const int klim = key_limit(p, b);
@@ -465,10 +470,20 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   }
 }
 
+// Heads per CTA group: K and V of a group within about 64 MB (half of L2).
+static int heads_per_group(long long heads, long long bytes_per_head) {
+  long long g = (64ll << 20) / (bytes_per_head > 0 ? bytes_per_head : 1);
+  if (g < 1) g = 1;
+  if (g > heads) g = heads;
+  return (int)g;
+}
+
 template <int D, bool PACKED, bool DROP>
-static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* k, const void* v,
-                                   void* o, float* lse, cudaStream_t st) {
+static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void* k,
+                                   const void* v, void* o, float* lse, cudaStream_t st) {
   using C = FwdTc<D>;
+  Problem p = pin;
+  p.hgroup = heads_per_group((long long)p.B * p.H, (long long)p.N * D * 4);
   const long long bh = (long long)p.B * p.H;
   CUtensorMap tq, tk, tv, to;
   bool maps;
@@ -485,7 +500,7 @@ static cudaError_t launch_fwd_tc_t(const Problem& p, const void* q, const void* 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)bh, (unsigned)((p.T + 1) / 2));
+  dim3 grid((unsigned)(bh * ((p.T + 1) / 2)));
   kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, to, p, lse,
                                           static_cast<__nv_bfloat16*>(o));
   return cudaGetLastError();

@@ -276,7 +276,8 @@ FA_API int fa_forward_varlen(const void* q, const void* k, const void* v, void* 
 
 /* Workspace of fa_backward_varlen: LSE*log2(e) and D per sequence row, padded
  * (fp32 [B*H][ceil(max_seqlen/128)*128] each), then the fp32 dQ accumulator
- * [total, H, d]; each part 256-byte aligned.  0 for invalid sizes. */
+ * [H, total, d] (head-major); each part 256-byte aligned.  0 for invalid
+ * sizes. */
 FA_API size_t fa_varlen_workspace_bytes(int B, int H, int total, int max_seqlen, int d);
 
 /* Backward of fa_forward_varlen (same sequences, mask and scale); launches
