@@ -1,5 +1,5 @@
 // Single-tile tensor-core self-test: exercises, one at a time, the operand
-// paths the attention kernels are built from (TMA with the 128-byte swizzle,
+// paths the attention kernels are built from (TMA with the 128- and 32-byte swizzles,
 // K-major and MN-major shared-memory descriptors, A staged in TMEM, TMEM
 // loads) on one 128-row tile, so a layout mistake shows up as a wrong
 // product here rather than as a wrong attention output.
@@ -50,7 +50,12 @@ __global__ void __launch_bounds__(128, 1)
 
   const int b_halves = (mode == 0) ? 2 : n / 64;
   if (threadIdx.x == 0) {
-    if (mode == 5) {
+    if (mode >= 6) {
+      // K = 16: one 32-byte-swizzled box of 16 columns per operand
+      mbar_expect_tx(bars, (mode == 7 ? 128 * 32 : 0) + n * 32);
+      if (mode == 7) tma_load_3d(sA, &tm_a, bars, 0, 0, 0);
+      tma_load_3d(sB, &tm_b, bars, 0, 0, 0);
+    } else if (mode == 5) {
       // 8-bit: one 128-byte-wide box of 128 rows per operand
       mbar_expect_tx(bars, 2 * kHalf);
       tma_load_3d(sA, &tm_a, bars, 0, 0, 0);
@@ -82,6 +87,12 @@ __global__ void __launch_bounds__(128, 1)
     }
     fence_proxy_async_smem();
   }
+  if (mode == 6) {
+    // A row r (first 16 columns) written by this thread in the 32-byte-swizzled layout
+    const uint4* src = reinterpret_cast<const uint4*>(a_glob + r * 128);
+    for (int ch = 0; ch < 2; ++ch) *reinterpret_cast<uint4*>(smem + sw32_offset(r, ch)) = src[ch];
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -89,7 +100,11 @@ __global__ void __launch_bounds__(128, 1)
   bool ok = mbar_wait(bars, 0, ab);
   if (ok && threadIdx.x == 0) {
     tc_fence_after();
-    if (mode == 5) {
+    if (mode >= 6) {
+      // c = a[:, :16] b[:, :16]^T: one MMA of depth 16, both operands K-major
+      // with the 32-byte swizzle (8-row groups 256 bytes apart)
+      mma_ss(tmem, sdesc_sw32(sA, 256), sdesc_sw32(sB, 256), idesc_bf16(128, n, false, false), 0);
+    } else if (mode == 5) {
       // c = a b^T with e4m3 operands, both K-major: K = 128 in four steps of
       // 32 elements (32 bytes) along the swizzled rows
       const uint32_t id = idesc_e4m3(128, 128);
@@ -144,10 +159,13 @@ using namespace fa;
 
 extern "C" int fa_selftest_mma(int mode, const void* a, const void* b, float* c, int n,
                                void* stream) {
-  if (mode < 0 || mode > 5 || !a || !b || !c) return 1;
+  if (mode < 0 || mode > 7 || !a || !b || !c) return 1;
   if (mode != 0 && mode != 5 && n != 64 && n != 128) return 1;
   CUtensorMap ta, tb;
-  if (mode == 5) {
+  if (mode >= 6) {
+    if (!make_bf16_map_sw32(&ta, a, 128, 128, 1, 128) || !make_bf16_map_sw32(&tb, b, 128, n, 1, n))
+      return 3;
+  } else if (mode == 5) {
     if (!make_u8_map_3d(&ta, a, 128, 128, 1, 128) || !make_u8_map_3d(&tb, b, 128, 128, 1, 128))
       return 3;
   } else {

@@ -238,6 +238,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor for a 32-byte-swizzled K-major operand (layout 6):
+// rows of 32 bytes (K = 16 bf16, one MMA's depth), 8-row groups `sbo` bytes
+// apart; within a group the two 16-byte halves of rows 4-7 trade places.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
+// Byte offset of 16-byte half `c` (0 or 1) of row r in a 32-byte-swizzled
+// K-major tile whose 8-row groups are 256 bytes apart.
+__host__ __device__ constexpr uint32_t sw32_offset(int r, int c) {
+  return (uint32_t)r * 32u + ((uint32_t)(c ^ ((r >> 2) & 1)) << 4);
+}
+
 
 // ---- GEMMs issued as one instruction sequence each (descriptor offsets
 // folded into immediates; the first MMA honours `acc`, the rest accumulate).

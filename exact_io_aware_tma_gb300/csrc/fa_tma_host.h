@@ -77,6 +77,23 @@ inline bool make_bf16_map_packed(CUtensorMap* m, const void* base, int cols, int
   return r == CUDA_SUCCESS;
 }
 
+// The first 16 columns of a bf16 tensor [heads][rows][row_elems], copied in
+// boxes of 16 columns (32 bytes) x box_rows rows with the 32-byte swizzle
+// (the layout of one K = 16 MMA operand).
+inline bool make_bf16_map_sw32(CUtensorMap* m, const void* base, int row_elems, int rows,
+                               long long heads, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)row_elems * 2, (cuuint64_t)row_elems * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {16, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // fp32 tensor viewed as [heads][rows][cols], boxes of cols x box_rows, no
 // swizzle (plain row-major tile in shared memory); used for reduce-adds.
 inline bool make_f32_map_3d(CUtensorMap* m, const void* base, int cols, int rows,

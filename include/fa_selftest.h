@@ -23,7 +23,12 @@
  *           path of the backward).
  *   mode 5: c = a * b^T with a, b e4m3 (8-bit float) [128][128] row-major,
  *           both K-major via TMA (the FP8 S = Q K^T and O += P V paths).
- *   n    : 64 or 128 (modes 1-4).
+ *   mode 6: c = a[:, :16] * b[:, :16]^T with b bf16 [n][128] row-major: one
+ *           MMA of depth 16, both operands K-major with the 32-byte swizzle,
+ *           a written to shared memory by threads, b via TMA (the row
+ *           statistic operand of the backward).
+ *   mode 7: as mode 6 with a also via TMA.
+ *   n    : 64 or 128 (modes 1-4, 6, 7).
  * Returns 0 on success, 1 on a bad argument, 3 on a CUDA error.  A bounded
  * wait that gives up is reported by fa_last_device_status().
  */

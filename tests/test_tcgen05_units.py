@@ -42,3 +42,18 @@ def test_single_tile_mma_e4m3():
     ref = a.to(torch.float64) @ b.to(torch.float64).T
     err = (c.double().cpu() - ref).abs().max().item()
     assert err <= 1e-5 * ref.abs().max().item() * 16, err
+
+
+@pytest.mark.parametrize("mode,n", [(6, 64), (6, 128), (7, 64), (7, 128)])
+def test_single_tile_mma_sw32_depth16(mode, n):
+    # modes 6/7: one MMA of depth 16 over 32-byte-swizzled K-major operands
+    # (a thread-written in mode 6, TMA-loaded in mode 7); c = a[:, :16] b[:, :16]^T
+    g = torch.Generator().manual_seed(700 + 10 * mode + n)
+    a = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    b = torch.randn(n, 128, generator=g).to(torch.bfloat16).cuda()
+    c = fa.selftest_mma(mode, a, b, n)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    ref = a[:, :16].double() @ b[:, :16].double().T
+    err = (c.double() - ref).abs().max().item()
+    assert err <= 1e-5 * ref.abs().max().item() * 16, (mode, n, err)
