@@ -67,7 +67,10 @@ struct BwdTc {
   // dropout keep bytes of a step, [64 queries][128 keys], two buffers
   static constexpr int OFF_DROP = (OFF_MISC + 32 + 127) / 128 * 128;
   static constexpr int DROPB = BQ * 128;
-  static constexpr int SMEM = OFF_DROP + 2 * DROPB + 1024;
+  // live query tiles of the key tile's range under a block mask, one bit each
+  static constexpr int OFF_LIVE = OFF_DROP + 2 * DROPB;
+  static constexpr int LIVEB = 65536 / 8;
+  static constexpr int SMEM = OFF_LIVE + LIVEB + 1024;
   static constexpr int COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(2 * KT <= NS * STAGE, "dK/dV staging must fit in the stage ring");
@@ -78,9 +81,12 @@ struct BwdTc {
 // in ascending order within the key tile's query-tile range (exact without a
 // block mask; recomputed here from the constant parameters rather than kept
 // live in registers across the roles' loops), two halves each, skipping
-// halves past N.
-__device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, int& qt,
-                                            int& sub) {
+// halves past N.  Under a block mask the live tiles come from `live`, bit t
+// for query tile first + t, built once per CTA: the mask's column of a key
+// tile is one byte per 128-byte line, so testing it per step from global
+// memory put a cache miss on every role's loop.
+__device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
+                                            const uint32_t* live, int& qt, int& sub) {
   if (qt >= 0 && sub == 0 && qt * 128 + 64 < p.N) {
     sub = 1;
     return true;
@@ -90,8 +96,15 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim, 
   ktile_query_tiles(p, kt, klim, qf, ql);
   qt = qt < 0 ? qf : qt + 1;
   if (p.block_mask == nullptr) return qt <= ql;
-  for (; qt <= ql; ++qt)
-    if (tile_live(p, qt, kt, klim)) return true;
+  while (qt <= ql) {
+    const int t = qt - qf;
+    const uint32_t w = live[t >> 5] >> (t & 31);  // bits past the range are 0
+    if (w != 0) {
+      qt += __ffs(w) - 1;
+      return true;
+    }
+    qt += 32 - (t & 31);
+  }
   return false;
 }
 
@@ -152,6 +165,17 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  if (p.block_mask != nullptr) {
+    // the range's liveness, 32 query tiles per warp and word, all warps at once
+    int qf, ql;
+    ktile_query_tiles(p, kt, klim, qf, ql);
+    const int n = ql - qf + 1;
+    for (int wi = warp; wi < ((n + 31) >> 5); wi += C::THREADS / 32) {
+      const int t = (wi << 5) + lane;
+      const uint32_t bits = __ballot_sync(0xffffffffu, t < n && tile_live(p, qf + t, kt, klim));
+      if (lane == 0) reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[wi] = bits;
+    }
+  }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
@@ -175,7 +199,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
                     cz(kt * 128));
       }
       int qt = -1, sub = 0, slot = 0, round = 0;
-      while (next_q_step(p, kt, klim, qt, sub)) {
+      while (next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub)) {
         const int q0 = qt * 128 + sub * 64;
         if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) break;
         const uint32_t st = s0 + C::OFF_ST + slot * C::STAGE;
@@ -231,7 +255,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       // The issuers need only the number of steps (descriptors depend on the
       // step index alone), so the walk is counted once up front.
       int nsteps = 0;
-      for (int qt = -1, sub = 0; next_q_step(p, kt, klim, qt, sub);) ++nsteps;
+      for (int qt = -1, sub = 0; next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub);) ++nsteps;
       bool ok = mbar_wait(bar(C::B_KV), 0, ab);
       tc_fence_after();
       if (warp == 1) {
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const float cl2 = p.scale_log2;
     int qt = -1, sub = 0, i = 0;
     bool ok = true;
-    for (; next_q_step(p, kt, klim, qt, sub); ++i) {
+    for (; next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       const uint8_t* vb = smem + C::OFF_VEC + (i % C::NS) * 512;
@@ -462,7 +486,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int qt = -1, sub = 0;
     bool ok = true;
-    for (int i = 0; next_q_step(p, kt, klim, qt, sub); ++i) {
+    for (int i = 0; next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab))) break;
