@@ -296,7 +296,9 @@ def run_gpu(args, cfg, name):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    wsb = fa.backward_workspace_bytes(B, H, N, d)
+    # with a block mask, room for the backward's split of heavy key tiles
+    wsb = fa.backward_workspace_bytes(B, H, N, d, bm)
+    split = wsb > fa.backward_workspace_bytes(B, H, N, d)
     ws = torch.empty(wsb, device=dev, dtype=torch.uint8)
     flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)  # > 129 MB L2
     lib = fa.load()
@@ -308,6 +310,7 @@ def run_gpu(args, cfg, name):
 
     def launch(i):
         # 4 launches of the library's kernels: fwd, preprocess, dK/dV(+dQ), dQ convert
+        # (5 with a split backward: its plan kernel runs before dK/dV)
         st = [lib.fa_forward(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, int(causal),
                              bmp, kvp, sp)]
         ev[i][1].record(stream)
@@ -460,7 +463,7 @@ def run_gpu(args, cfg, name):
                          "peak_kind": peak_kind, "traffic": traffic_record(dom)},
             "cpu_baseline": cpu_base,
             "e2e": e2e,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": (5 if split else 4) * args.steps,
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "kvcache_decode": kvc,

@@ -336,6 +336,24 @@ size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   return 2 * vec + round_up((size_t)B * H * N * d * sizeof(float), 256);
 }
 
+// Extra workspace of the split backward (block masks): the plan's items and
+// count, the slot counters and the fp32 slots; 0 where it does not apply.
+static size_t split_bytes(const Problem& p) {
+  const long long heads = (long long)p.B * p.H;
+  if (p.block_mask == nullptr || p.T > kPlanMaxTiles ||
+      heads * p.T * kSplitMax > 2147483647LL)
+    return 0;
+  return round_up((size_t)p.T * kSplitMax * sizeof(int4), 256) + 256 +
+         round_up((size_t)heads * kSplitSlots * sizeof(int), 256) +
+         (size_t)heads * kSplitSlots * 2 * 128 * p.d * sizeof(float);
+}
+
+size_t fa_backward_workspace_bytes_masked(int B, int H, int N, int d, const fa_mask* mask) {
+  Problem p;
+  if (check_sizes(B, H, N, d, 1.0f, mask, &p) != FA_OK) return 0;
+  return fa_backward_workspace_bytes(B, H, N, d) + split_bytes(p);
+}
+
 static int check_workspace(int B, int H, int N, int d, const void* ws, size_t wsb) {
   if (!ws || !aligned(ws, 256)) return FA_ERR_INVALID_ARG;
   if (wsb < fa_backward_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
@@ -403,9 +421,25 @@ static int backward_dkdv(const void* q, const void* k, const void* v, const void
   p.status = status_word();
   if (p.status == nullptr) return FA_ERR_CUDA;
   const long long heads = (long long)B * H;
+  // Block mask and room for the split's extra workspace: key tiles with many
+  // live query tiles are spread over several CTAs.
+  BwdSplit split{};
+  const size_t base = fa_backward_workspace_bytes(B, H, N, d), extra = split_bytes(p);
+  const bool use_split = extra != 0 && workspace_bytes >= base + extra;
+  if (use_split) {
+    char* w = static_cast<char*>(workspace) + base;
+    split.items = reinterpret_cast<const int4*>(w);
+    w += round_up((size_t)p.T * kSplitMax * sizeof(int4), 256);
+    split.nitems = reinterpret_cast<const int*>(w);
+    w += 256;
+    split.counters = reinterpret_cast<int*>(w);
+    w += round_up((size_t)heads * kSplitSlots * sizeof(int), 256);
+    split.slots = reinterpret_cast<float*>(w);
+  }
   cudaError_t e = launch_bwd_tc(p, q, k, v, dout, ws_lse2(workspace),
                                 ws_dvec(workspace, heads, N), ws_dq_acc(workspace, heads, N),
-                                dk, dv, padded_rows(N), static_cast<cudaStream_t>(stream));
+                                dk, dv, padded_rows(N), use_split ? &split : nullptr,
+                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -568,7 +602,7 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
                                                            cu_seqlens, H, heads, total,
                                                            max_seqlen, npad);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  cudaError_t e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, s);
+  cudaError_t e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, nullptr, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   const long long chunks = (long long)total * H * (d / 8);
   dq_convert_packed_kernel<<<elementwise_blocks(chunks), 256, 0, s>>>(

@@ -64,8 +64,10 @@ struct BwdTc {
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
                        B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  // misc: TMEM address (+0), abort flag (+16), split range (+32, +36) and
+  // last-part flag (+40)
   // dropout keep bytes of a step, [64 queries][128 keys], two buffers
-  static constexpr int OFF_DROP = (OFF_MISC + 32 + 127) / 128 * 128;
+  static constexpr int OFF_DROP = (OFF_MISC + 64 + 127) / 128 * 128;
   static constexpr int DROPB = BQ * 128;
   // live query tiles of the key tile's range under a block mask, one bit each
   static constexpr int OFF_LIVE = OFF_DROP + 2 * DROPB;
@@ -85,17 +87,26 @@ struct BwdTc {
 // for query tile first + t, built once per CTA: the mask's column of a key
 // tile is one byte per 128-byte line, so testing it per step from global
 // memory put a cache miss on every role's loop.
+// A CTA of the split variant walks only its part [qf, ql] of the range (kept
+// in shared memory).
+template <int D, bool SPLIT>
 __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
-                                            const uint32_t* live, int& qt, int& sub) {
+                                            const uint8_t* smem, int& qt, int& sub) {
   if (qt >= 0 && sub == 0 && qt * 128 + 64 < p.N) {
     sub = 1;
     return true;
   }
   sub = 0;
   int qf, ql;
-  ktile_query_tiles(p, kt, klim, qf, ql);
+  if constexpr (SPLIT) {
+    qf = reinterpret_cast<const int*>(smem + BwdTc<D>::OFF_MISC)[8];
+    ql = reinterpret_cast<const int*>(smem + BwdTc<D>::OFF_MISC)[9];
+  } else {
+    ktile_query_tiles(p, kt, klim, qf, ql);
+  }
   qt = qt < 0 ? qf : qt + 1;
-  if (p.block_mask == nullptr) return qt <= ql;
+  if (!SPLIT && p.block_mask == nullptr) return qt <= ql;
+  const uint32_t* live = reinterpret_cast<const uint32_t*>(smem + BwdTc<D>::OFF_LIVE);
   while (qt <= ql) {
     const int t = qt - qf;
     const uint32_t w = live[t >> 5] >> (t & 31);  // bits past the range are 0
@@ -108,14 +119,14 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
   return false;
 }
 
-template <int D, bool PACKED, bool DROP>
+template <int D, bool PACKED, bool DROP, bool SPLIT>
 __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   const Problem pin, const float* __restrict__ lse2, const float* __restrict__ dvec,
                   float* __restrict__ dq_acc, int npad, __nv_bfloat16* __restrict__ dk_rows,
-                  __nv_bfloat16* __restrict__ dv_rows) {
+                  __nv_bfloat16* __restrict__ dv_rows, const BwdSplit sp) {
   using C = BwdTc<D>;
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
@@ -123,9 +134,20 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   // Grid: one CTA per (head, key tile) in the grouped order -- small key
   // tiles carry the most causal work: first, across a group of heads whose
   // Q, dO and dQ accumulator stay in L2.
+  // Split variant: CTA rank r of a head runs work item r of the plan (key
+  // tile, part [qa, qb] of its query range, part k of n), heaviest first.
   long long bh;
   int kt;
-  grouped_cta(pin, blockIdx.x, pin.T, bh, kt);
+  int4 item = make_int4(0, 0, -1, 1 << 8);
+  if constexpr (SPLIT) {
+    int r;
+    grouped_cta(pin, blockIdx.x, pin.T * kSplitMax, bh, r);
+    if (r >= __ldg(sp.nitems)) return;
+    item = __ldg(sp.items + r);
+    kt = item.x;
+  } else {
+    grouped_cta(pin, blockIdx.x, pin.T, bh, kt);
+  }
   const int b = (int)(bh / pin.H);
   const int head = (int)(bh % pin.H);
   Problem p = pin;
@@ -169,6 +191,14 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     // the range's liveness, 32 query tiles per warp and word, all warps at once
     int qf, ql;
     ktile_query_tiles(p, kt, klim, qf, ql);
+    if constexpr (SPLIT) {
+      qf = max(qf, item.y);
+      ql = min(ql, item.z);
+      if (threadIdx.x == 0) {
+        reinterpret_cast<int*>(smem + C::OFF_MISC)[8] = qf;
+        reinterpret_cast<int*>(smem + C::OFF_MISC)[9] = ql;
+      }
+    }
     const int n = ql - qf + 1;
     for (int wi = warp; wi < ((n + 31) >> 5); wi += C::THREADS / 32) {
       const int t = (wi << 5) + lane;
@@ -199,7 +229,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
                     cz(kt * 128));
       }
       int qt = -1, sub = 0, slot = 0, round = 0;
-      while (next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub)) {
+      while (next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub)) {
         const int q0 = qt * 128 + sub * 64;
         if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) break;
         const uint32_t st = s0 + C::OFF_ST + slot * C::STAGE;
@@ -255,7 +285,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       // The issuers need only the number of steps (descriptors depend on the
       // step index alone), so the walk is counted once up front.
       int nsteps = 0;
-      for (int qt = -1, sub = 0; next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub);) ++nsteps;
+      for (int qt = -1, sub = 0; next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub);) ++nsteps;
       bool ok = mbar_wait(bar(C::B_KV), 0, ab);
       tc_fence_after();
       if (warp == 1) {
@@ -313,7 +343,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const float cl2 = p.scale_log2;
     int qt = -1, sub = 0, i = 0;
     bool ok = true;
-    for (; next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub); ++i) {
+    for (; next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       const uint8_t* vb = smem + C::OFF_VEC + (i % C::NS) * 512;
@@ -433,16 +463,74 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     // sequence's first rows).
     if (ok) ok = mbar_wait(bar(C::B_FIN), 0, ab);
     tc_fence_after();
+    // Split key tile (part k of n): every part stores its fp32 dK, dV rows
+    // into its own slot; the part that finishes last (a counter per key
+    // tile, after a fence) sums the n slots and writes the result below.
+    int nparts = 1;
+    const float* slot0 = nullptr;
+    bool emit = true;
+    if constexpr (SPLIT) {
+      nparts = (item.w >> 8) & 0xff;
+      if (nparts > 1) {
+        const int part = item.w & 0xff, sidx = item.w >> 16;
+        const size_t sbase = (size_t)bh * kSplitSlots + sidx;
+        float* mine = sp.slots + ((sbase + part) * 2 * 128 + r) * D;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (i > 0 && ok) {
+              tmem_ld32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<uint4*>(mine + t * 128 * D + 32 * c)[e] =
+                  make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          }
+        }
+        __threadfence();
+        named_barrier(1, 128);
+        volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 40);
+        if (r == 0) *last_flag = atomicAdd(sp.counters + sbase, 1) == nparts - 1;
+        named_barrier(1, 128);
+        emit = *last_flag != 0;
+        __threadfence();
+        slot0 = sp.slots + (sbase * 2 * 128 + r) * D;
+      }
+    }
     uint8_t* stg = smem + C::OFF_ST;  // dK tile, then dV tile
     const bool direct = PACKED && (kt + 1) * 128 > p.N;
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < 2 && emit; ++t) {
       const uint32_t col = t == 0 ? C::COL_DK : C::COL_DV;
       const float mul = t == 0 ? p.scale : 1.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        if (i > 0 && ok) {
+        if (SPLIT && nparts > 1) {
+          // the parts' slots, read from L2 (written by other SMs)
+          float acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+          for (int k2 = 0; k2 < nparts; ++k2) {
+            const float4* src =
+                reinterpret_cast<const float4*>(slot0 + ((size_t)k2 * 2 * 128 + t * 128) * D + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 x = __ldcg(src + e);
+              acc[4 * e] += x.x;
+              acc[4 * e + 1] += x.y;
+              acc[4 * e + 2] += x.z;
+              acc[4 * e + 3] += x.w;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(acc[e]);
+        } else if (i > 0 && ok) {
           tmem_ld32(lane_base + col + 32 * c, o);
         } else {
 #pragma unroll
@@ -470,7 +558,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     }
     fence_proxy_async_smem();
     named_barrier(1, 128);
-    if (ok && r == 0 && !direct) {
+    if (ok && emit && r == 0 && !direct) {
       for (int h = 0; h < D / 64; ++h) {
         tma_store_3d(&tm_dk, smem_u32(stg) + h * C::HALF_K, h * 64, cy(kt * 128), cz(kt * 128));
         tma_store_3d(&tm_dv, smem_u32(stg) + C::KT + h * C::HALF_K, h * 64, cy(kt * 128),
@@ -486,7 +574,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int qt = -1, sub = 0;
     bool ok = true;
-    for (int i = 0; next_q_step(p, kt, klim, reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE), qt, sub); ++i) {
+    for (int i = 0; next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab))) break;
@@ -520,11 +608,102 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   }
 }
 
-template <int D, bool PACKED, bool DROP>
+// Work plan of the split backward, one CTA.  Per key tile, c = its live
+// query tiles (block mask, causal rule, window; the per-batch key limit is
+// left to the kernel, which only drops tiles from a part).  With a = the
+// average work per SM, max(2, ceil(B*H*sum(c) / nsm)), a key tile with
+// c > a runs as n = min(kSplitMax, ceil(c / a)) parts of consecutive live
+// tiles (a doubles until the split tiles' parts fit kSplitSlots slots per
+// head).  Items are ordered by their number of live tiles, heaviest first;
+// the counters of the slots are cleared.
+__global__ void __launch_bounds__(1024)
+    bwd_plan_kernel(const Problem p, int nsm, long long heads, int4* __restrict__ items,
+                    int* __restrict__ nitems, int* __restrict__ counters) {
+  __shared__ int cnt[kPlanMaxTiles];
+  __shared__ int meta[kPlanMaxTiles];  // n | slot base << 16
+  __shared__ int hist[kPlanMaxTiles + 2];
+  __shared__ unsigned long long tot;
+  __shared__ int slots, next_base;
+  const int T = p.T, tid = threadIdx.x, nth = blockDim.x;
+  if (tid == 0) {
+    tot = 0;
+    next_base = 0;
+  }
+  for (int w = tid; w <= T + 1; w += nth) hist[w] = 0;
+  __syncthreads();
+  for (int kt = tid; kt < T; kt += nth) {
+    int qf, ql;
+    ktile_query_tiles(p, kt, p.N, qf, ql);
+    int c = 0;
+    for (int qt = qf; qt <= ql; ++qt) c += tile_live(p, qt, kt, p.N) ? 1 : 0;
+    cnt[kt] = c;
+    atomicAdd(&tot, (unsigned long long)c);
+  }
+  __syncthreads();
+  long long a = ((long long)tot * heads + nsm - 1) / nsm;
+  if (a < 2) a = 2;
+  auto parts = [&](int c) {
+    return c > a ? (int)min((long long)kSplitMax, (c + a - 1) / a) : 1;
+  };
+  for (;;) {
+    if (tid == 0) slots = 0;
+    __syncthreads();
+    for (int kt = tid; kt < T; kt += nth) {
+      const int n = parts(cnt[kt]);
+      if (n > 1) atomicAdd(&slots, n);
+    }
+    __syncthreads();
+    const bool fits = slots <= kSplitSlots;
+    __syncthreads();
+    if (fits) break;
+    a *= 2;
+  }
+  for (int kt = tid; kt < T; kt += nth) {
+    const int c = cnt[kt], n = parts(c);
+    meta[kt] = n | ((n > 1 ? atomicAdd(&next_base, n) : 0) << 16);
+    for (int k = 0; k < n; ++k) atomicAdd(&hist[(k + 1) * c / n - k * c / n], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {  // first position of each weight, heaviest first
+    int pos = 0;
+    for (int w = T; w >= 0; --w) {
+      const int h = hist[w];
+      hist[w] = pos;
+      pos += h;
+    }
+    *nitems = pos;
+  }
+  __syncthreads();
+  for (int kt = tid; kt < T; kt += nth) {
+    const int c = cnt[kt], n = meta[kt] & 0xffff, sbase = meta[kt] >> 16;
+    int qf, ql;
+    ktile_query_tiles(p, kt, p.N, qf, ql);
+    int qt = qf, li = 0;  // next candidate tile; live index the next live tile gets
+    for (int k = 0; k < n; ++k) {
+      const int lo = k * c / n, hi = (k + 1) * c / n;  // live indices [lo, hi)
+      int qa = 0, qb = -1;
+      if (hi > lo) {
+        for (; qt <= ql; ++qt)
+          if (tile_live(p, qt, kt, p.N)) break;
+        qa = qb = qt;
+        ++li;
+        for (++qt; li < hi && qt <= ql; ++qt)
+          if (tile_live(p, qt, kt, p.N)) {
+            qb = qt;
+            ++li;
+          }
+      }
+      items[atomicAdd(&hist[hi - lo], 1)] = make_int4(kt, qa, qb, k | (n << 8) | (sbase << 16));
+    }
+  }
+  for (long long i = tid; i < heads * kSplitSlots; i += nth) counters[i] = 0;
+}
+
+template <int D, bool PACKED, bool DROP, bool SPLIT>
 static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void* k,
                                    const void* v, const void* dout, const float* lse2,
                                    const float* dvec, float* dq_acc, void* dk, void* dv, int npad,
-                                   cudaStream_t st) {
+                                   const BwdSplit& split, cudaStream_t st) {
   using C = BwdTc<D>;
   // Heads per CTA group: Q, dO (bf16) and the fp32 dQ accumulator of a group
   // within about 64 MB (half of L2).
@@ -550,38 +729,59 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
            make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) &&
            make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) && make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128);
   if (!maps) return cudaErrorInvalidValue;
-  auto kern = bwd_tc_kernel<D, PACKED, DROP>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e;
+  if constexpr (SPLIT) {
+    static int nsm = 0;
+    if (nsm == 0) {
+      int dev = 0;
+      if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+      if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    }
+    bwd_plan_kernel<<<1, 1024, 0, st>>>(p, nsm, bh, const_cast<int4*>(split.items),
+                                        const_cast<int*>(split.nitems), split.counters);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(bh * p.T));
+  dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
   kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad,
                                           static_cast<__nv_bfloat16*>(dk),
-                                          static_cast<__nv_bfloat16*>(dv));
+                                          static_cast<__nv_bfloat16*>(dv), split);
   return cudaGetLastError();
 }
 
-template <bool PACKED, bool DROP>
+template <bool PACKED, bool DROP, bool SPLIT>
 static cudaError_t launch_bwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
                                    const void* dout, const float* lse2, const float* dvec,
-                                   float* dq_acc, void* dk, void* dv, int npad, cudaStream_t st) {
-  return p.d == 64 ? launch_bwd_tc_t<64, PACKED, DROP>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
-                                                       dv, npad, st)
-                   : launch_bwd_tc_t<128, PACKED, DROP>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
-                                                        dv, npad, st);
+                                   float* dq_acc, void* dk, void* dv, int npad,
+                                   const BwdSplit& split, cudaStream_t st) {
+  return p.d == 64 ? launch_bwd_tc_t<64, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
+                                                              dq_acc, dk, dv, npad, split, st)
+                   : launch_bwd_tc_t<128, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
+                                                               dq_acc, dk, dv, npad, split, st);
 }
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
-                          void* dk, void* dv, int npad, cudaStream_t st) {
+                          void* dk, void* dv, int npad, const BwdSplit* split, cudaStream_t st) {
   const bool packed = p.cu_seqlens != nullptr, drop = p.drop_p8 != 0;
+  const BwdSplit none{nullptr, nullptr, nullptr, nullptr};
   if (packed)
-    return drop ? launch_bwd_tc_d<true, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
-                : launch_bwd_tc_d<true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad,
-                                               st);
-  return drop ? launch_bwd_tc_d<false, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, st)
-              : launch_bwd_tc_d<false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad,
-                                              st);
+    return drop ? launch_bwd_tc_d<true, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
+                                                     npad, none, st)
+                : launch_bwd_tc_d<true, false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
+                                                      dv, npad, none, st);
+  if (split != nullptr)
+    return drop ? launch_bwd_tc_d<false, true, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
+                                                     npad, *split, st)
+                : launch_bwd_tc_d<false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
+                                                      dv, npad, *split, st);
+  return drop ? launch_bwd_tc_d<false, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
+                                                    npad, none, st)
+              : launch_bwd_tc_d<false, false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
+                                                     npad, none, st);
 }
 
 }  // namespace fa

@@ -73,6 +73,21 @@ __device__ __forceinline__ uint32_t keep4(uint32_t w, uint32_t p8) {
          (((w >> 16) & 0xffu) >= p8 ? 4u : 0u) | ((w >> 24) >= p8 ? 8u : 0u);
 }
 
+// Backward work split of key tiles with many live query tiles (block
+// masks): up to kSplitMax parts per key tile, kSplitSlots part slots per
+// head, planned for at most kPlanMaxTiles key tiles.
+constexpr int kSplitMax = 4;
+constexpr int kSplitSlots = 32;
+constexpr int kPlanMaxTiles = 2048;
+// The plan and the slots a split backward reads and writes (device
+// pointers into the caller's workspace).
+struct BwdSplit {
+  const int4* items;  // [T * kSplitMax] work items, heaviest first
+  const int* nitems;  // number of items
+  int* counters;      // [B*H][kSplitSlots] finished parts per split key tile
+  float* slots;       // [B*H][kSplitSlots][2][128][d] fp32 partial dK, dV rows
+};
+
 // Head and tile rank of CTA `cta` of a grid of B*H x ntiles CTAs in the
 // grouped order above (the last group may hold fewer heads).
 __device__ __forceinline__ void grouped_cta(const Problem& p, long long cta, int ntiles,

@@ -12,9 +12,12 @@ cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const 
 
 int* status_word();
 
+// split != nullptr (padded layout with a block mask): the work of key tiles
+// with many live query tiles is spread over several CTAs by a plan kernel
+// launched first (BwdSplit in fa_common.cuh).
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
-                          void* dk, void* dv, int npad, cudaStream_t st);
+                          void* dk, void* dv, int npad, const BwdSplit* split, cudaStream_t st);
 
 // e4m3 forward (d = 128) on quantised operands: q8, k8 [B*H][N][128],
 // vt8 [B*H][128][ceil(N/128)*128], q/k scales [B*H][T], v scale [B*H].

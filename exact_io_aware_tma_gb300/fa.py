@@ -24,6 +24,7 @@ SIGNATURES = {
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_forward": ([_vp] * 5 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
     "fa_backward_workspace_bytes": ([_i] * 4, _sz),
+    "fa_backward_workspace_bytes_masked": ([_i] * 4 + [_vp], _sz),
     "fa_backward": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_backward_preprocess": ([_vp, _vp, _vp] + [_i] * 4 + [_vp, _sz, _vp], _i),
     "fa_backward_dkdv": ([_vp] * 6 + [_i] * 4 + [_f, _i, _vp, _vp, _vp, _sz, _vp], _i),
@@ -153,8 +154,13 @@ def forward(q, k, v, causal=False, block_mask=None, kv_len=None, scale=None,
     return out, lse
 
 
-def backward_workspace_bytes(B, H, N, d):
-    return int(load().fa_backward_workspace_bytes(B, H, N, d))
+def backward_workspace_bytes(B, H, N, d, block_mask=None):
+    """Workspace of a backward call; with a block mask, the larger size that
+    lets the backward split heavy key tiles (``fa_backward_workspace_bytes_masked``)."""
+    if block_mask is None:
+        return int(load().fa_backward_workspace_bytes(B, H, N, d))
+    m = _mask(N, False, block_mask, None, B, None)
+    return int(load().fa_backward_workspace_bytes_masked(B, H, N, d, ctypes.byref(m)))
 
 
 def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
@@ -165,7 +171,7 @@ def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
     _check_qkv(q, k, v, o, do)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    nbytes = backward_workspace_bytes(B, H, N, d)
+    nbytes = backward_workspace_bytes(B, H, N, d, block_mask)
     if workspace is None:
         workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
     dq = torch.empty_like(q) if dq is None else dq

@@ -140,6 +140,24 @@ FA_API int fa_forward_masked(const void* q, const void* k, const void* v, void* 
 FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * Workspace for a backward call with `mask` (NULL = no mask).  With a block
+ * mask (and N <= 262,144, B*H*ceil(N/128)*4 < 2^31) this adds room for
+ * spreading the work of a key tile over up to 4 CTAs: a key tile with many
+ * live query tiles (a global column, say) otherwise walks all of them in one
+ * CTA while the GPU idles.  The extra part holds a work plan
+ * (16 * 4 * ceil(N/128) bytes), 32 counters per head and 32 fp32 slots of
+ * 2 x 128 x d values per head (1 KiB x d each), about B*H*d*32 KiB in all.  Given
+ * a workspace of at least this size, fa_backward_masked / fa_backward /
+ * fa_backward_dkdv launch a small planning kernel before the dK/dV kernel
+ * and split heavy key tiles (each split key tile's partial dK, dV rows meet
+ * in the slots and the part that finishes last writes the sum); with only
+ * fa_backward_workspace_bytes() they do not split.  Results agree up to the
+ * order of fp32 additions.  Returns 0 for invalid sizes.
+ */
+FA_API size_t fa_backward_workspace_bytes_masked(int B, int H, int N, int d,
+                                                 const fa_mask* mask);
+
+/*
  * Backward pass: dQ, dK, dV of L = sum(O * dO), recomputing P tile by tile
  * from Q, K and the forward's LSE (P is never stored).
  *   q, k, v, o : forward inputs and output, bf16 [B,H,N,d].
