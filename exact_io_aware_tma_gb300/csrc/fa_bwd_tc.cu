@@ -64,8 +64,8 @@ struct BwdTc {
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
                        B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  // misc: TMEM address (+0), abort flag (+16), split range (+32, +36) and
-  // last-part flag (+40)
+  // misc: TMEM address (+0), abort flag (+16), last-part flag (+40) and the
+  // split item's part word (+44)
   // dropout keep bytes of a step, [64 queries][128 keys], two buffers
   static constexpr int OFF_DROP = (OFF_MISC + 64 + 127) / 128 * 128;
   static constexpr int DROPB = BQ * 128;
@@ -87,9 +87,9 @@ struct BwdTc {
 // for query tile first + t, built once per CTA: the mask's column of a key
 // tile is one byte per 128-byte line, so testing it per step from global
 // memory put a cache miss on every role's loop.
-// A CTA of the split variant walks only its part [qf, ql] of the range (kept
-// in shared memory).
-template <int D, bool SPLIT>
+// (A CTA of the split variant runs one part of a key tile's live tiles: the
+// bitmask then holds only that part's bits.)
+template <int D>
 __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
                                             const uint8_t* smem, int& qt, int& sub) {
   if (qt >= 0 && sub == 0 && qt * 128 + 64 < p.N) {
@@ -98,14 +98,9 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
   }
   sub = 0;
   int qf, ql;
-  if constexpr (SPLIT) {
-    qf = reinterpret_cast<const int*>(smem + BwdTc<D>::OFF_MISC)[8];
-    ql = reinterpret_cast<const int*>(smem + BwdTc<D>::OFF_MISC)[9];
-  } else {
-    ktile_query_tiles(p, kt, klim, qf, ql);
-  }
+  ktile_query_tiles(p, kt, klim, qf, ql);
   qt = qt < 0 ? qf : qt + 1;
-  if (!SPLIT && p.block_mask == nullptr) return qt <= ql;
+  if (p.block_mask == nullptr) return qt <= ql;
   const uint32_t* live = reinterpret_cast<const uint32_t*>(smem + BwdTc<D>::OFF_LIVE);
   while (qt <= ql) {
     const int t = qt - qf;
@@ -192,17 +187,14 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     int qf, ql;
     ktile_query_tiles(p, kt, klim, qf, ql);
     if constexpr (SPLIT) {
-      qf = max(qf, item.y);
-      ql = min(ql, item.z);
-      if (threadIdx.x == 0) {
-        reinterpret_cast<int*>(smem + C::OFF_MISC)[8] = qf;
-        reinterpret_cast<int*>(smem + C::OFF_MISC)[9] = ql;
-      }
+      if (threadIdx.x == 0) reinterpret_cast<int*>(smem + C::OFF_MISC)[11] = item.w;
     }
     const int n = ql - qf + 1;
     for (int wi = warp; wi < ((n + 31) >> 5); wi += C::THREADS / 32) {
       const int t = (wi << 5) + lane;
-      const uint32_t bits = __ballot_sync(0xffffffffu, t < n && tile_live(p, qf + t, kt, klim));
+      const bool in_part = !SPLIT || (qf + t >= item.y && qf + t <= item.z);
+      const uint32_t bits =
+          __ballot_sync(0xffffffffu, t < n && in_part && tile_live(p, qf + t, kt, klim));
       if (lane == 0) reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[wi] = bits;
     }
   }
@@ -229,7 +221,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
                     cz(kt * 128));
       }
       int qt = -1, sub = 0, slot = 0, round = 0;
-      while (next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub)) {
+      while (next_q_step<D>(p, kt, klim, smem, qt, sub)) {
         const int q0 = qt * 128 + sub * 64;
         if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) break;
         const uint32_t st = s0 + C::OFF_ST + slot * C::STAGE;
@@ -285,7 +277,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       // The issuers need only the number of steps (descriptors depend on the
       // step index alone), so the walk is counted once up front.
       int nsteps = 0;
-      for (int qt = -1, sub = 0; next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub);) ++nsteps;
+      for (int qt = -1, sub = 0; next_q_step<D>(p, kt, klim, smem, qt, sub);) ++nsteps;
       bool ok = mbar_wait(bar(C::B_KV), 0, ab);
       tc_fence_after();
       if (warp == 1) {
@@ -343,7 +335,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const float cl2 = p.scale_log2;
     int qt = -1, sub = 0, i = 0;
     bool ok = true;
-    for (; next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub); ++i) {
+    for (; next_q_step<D>(p, kt, klim, smem, qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       const uint8_t* vb = smem + C::OFF_VEC + (i % C::NS) * 512;
@@ -470,9 +462,11 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const float* slot0 = nullptr;
     bool emit = true;
     if constexpr (SPLIT) {
-      nparts = (item.w >> 8) & 0xff;
+      // the item's part word, kept in shared memory through the loops
+      const int meta = reinterpret_cast<const volatile int*>(smem + C::OFF_MISC)[11];
+      nparts = (meta >> 8) & 0xff;
       if (nparts > 1) {
-        const int part = item.w & 0xff, sidx = item.w >> 16;
+        const int part = meta & 0xff, sidx = meta >> 16;
         const size_t sbase = (size_t)bh * kSplitSlots + sidx;
         float* mine = sp.slots + ((sbase + part) * 2 * 128 + r) * D;
 #pragma unroll
@@ -574,7 +568,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int qt = -1, sub = 0;
     bool ok = true;
-    for (int i = 0; next_q_step<D, SPLIT>(p, kt, klim, smem, qt, sub); ++i) {
+    for (int i = 0; next_q_step<D>(p, kt, klim, smem, qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab))) break;
