@@ -604,35 +604,39 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
 
 // Work plan of the split backward, one CTA.  Per key tile, c = its live
 // query tiles (block mask, causal rule, window; the per-batch key limit is
-// left to the kernel, which only drops tiles from a part).  With a = the
-// average work per SM, max(2, ceil(B*H*sum(c) / nsm)), a key tile with
-// c > a runs as n = min(kSplitMax, ceil(c / a)) parts of consecutive live
-// tiles (a doubles until the split tiles' parts fit kSplitSlots slots per
-// head).  Items are ordered by their number of live tiles, heaviest first;
-// the counters of the slots are cleared.
+// left to the kernel, which only drops tiles from a part), counted from a
+// row-major (coalesced) pass over the mask.  With a = the average work per
+// SM, max(2, ceil(B*H*sum(c) / nsm)), a key tile with c > a runs as
+// n = min(kSplitMax, ceil(c / a)) parts of consecutive live tiles (a doubles
+// until the split tiles' parts fit kSplitSlots slots per head); part k
+// starts at the query tile holding live tile k*c/n, found by one warp per
+// split key tile.  Items are ordered by their number of live tiles,
+// heaviest first; the slot counters are cleared.
 __global__ void __launch_bounds__(1024)
     bwd_plan_kernel(const Problem p, int nsm, long long heads, int4* __restrict__ items,
                     int* __restrict__ nitems, int* __restrict__ counters) {
   __shared__ int cnt[kPlanMaxTiles];
   __shared__ int meta[kPlanMaxTiles];  // n | slot base << 16
   __shared__ int hist[kPlanMaxTiles + 2];
+  __shared__ int start[kSplitSlots];  // first query tile of each part of a split key tile
+  __shared__ int split_kt[kSplitSlots];
   __shared__ unsigned long long tot;
-  __shared__ int slots, next_base;
+  __shared__ int slots, next_base, nsplit;
   const int T = p.T, tid = threadIdx.x, nth = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     tot = 0;
     next_base = 0;
+    nsplit = 0;
   }
+  for (int w = tid; w < T; w += nth) cnt[w] = 0;
   for (int w = tid; w <= T + 1; w += nth) hist[w] = 0;
   __syncthreads();
-  for (int kt = tid; kt < T; kt += nth) {
-    int qf, ql;
-    ktile_query_tiles(p, kt, p.N, qf, ql);
-    int c = 0;
-    for (int qt = qf; qt <= ql; ++qt) c += tile_live(p, qt, kt, p.N) ? 1 : 0;
-    cnt[kt] = c;
-    atomicAdd(&tot, (unsigned long long)c);
-  }
+  for (int qt = warp; qt < T; qt += nth / 32)
+    for (int kt = lane; kt < T; kt += 32)
+      if (tile_live(p, qt, kt, p.N)) atomicAdd(&cnt[kt], 1);
+  __syncthreads();
+  for (int kt = tid; kt < T; kt += nth) atomicAdd(&tot, (unsigned long long)cnt[kt]);
   __syncthreads();
   long long a = ((long long)tot * heads + nsm - 1) / nsm;
   if (a < 2) a = 2;
@@ -654,10 +658,33 @@ __global__ void __launch_bounds__(1024)
   }
   for (int kt = tid; kt < T; kt += nth) {
     const int c = cnt[kt], n = parts(c);
-    meta[kt] = n | ((n > 1 ? atomicAdd(&next_base, n) : 0) << 16);
+    int base = 0;
+    if (n > 1) {
+      base = atomicAdd(&next_base, n);
+      split_kt[atomicAdd(&nsplit, 1)] = kt;
+    }
+    meta[kt] = n | (base << 16);
     for (int k = 0; k < n; ++k) atomicAdd(&hist[(k + 1) * c / n - k * c / n], 1);
   }
   __syncthreads();
+  // part starts of the split key tiles: warp w scans key tile split_kt[w]'s
+  // column 32 query tiles at a time, counting live tiles with ballots
+  for (int sk = warp; sk < nsplit; sk += nth / 32) {
+    const int kt = split_kt[sk], c = cnt[kt], n = meta[kt] & 0xffff, base = meta[kt] >> 16;
+    int k = 1, seen = 0;
+    for (int q0 = 0; q0 < T && k < n; q0 += 32) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, q0 + lane < T && tile_live(p, q0 + lane, kt, p.N));
+      const int nb = __popc(bits);
+      while (k < n && seen + nb > k * c / n) {
+        // the (k*c/n - seen)-th set bit of this chunk
+        uint32_t b = bits;
+        for (int skip = k * c / n - seen; skip > 0; --skip) b &= b - 1;
+        if (lane == 0) start[base + k] = q0 + __ffs(b) - 1;
+        ++k;
+      }
+      seen += nb;
+    }
+  }
   if (tid == 0) {  // first position of each weight, heaviest first
     int pos = 0;
     for (int w = T; w >= 0; --w) {
@@ -668,26 +695,15 @@ __global__ void __launch_bounds__(1024)
     *nitems = pos;
   }
   __syncthreads();
+  // items: the whole range [0, T-1] for an unsplit key tile (the kernel
+  // walks its live tiles), consecutive query-tile ranges for the parts
   for (int kt = tid; kt < T; kt += nth) {
-    const int c = cnt[kt], n = meta[kt] & 0xffff, sbase = meta[kt] >> 16;
-    int qf, ql;
-    ktile_query_tiles(p, kt, p.N, qf, ql);
-    int qt = qf, li = 0;  // next candidate tile; live index the next live tile gets
+    const int c = cnt[kt], n = meta[kt] & 0xffff, base = meta[kt] >> 16;
     for (int k = 0; k < n; ++k) {
-      const int lo = k * c / n, hi = (k + 1) * c / n;  // live indices [lo, hi)
-      int qa = 0, qb = -1;
-      if (hi > lo) {
-        for (; qt <= ql; ++qt)
-          if (tile_live(p, qt, kt, p.N)) break;
-        qa = qb = qt;
-        ++li;
-        for (++qt; li < hi && qt <= ql; ++qt)
-          if (tile_live(p, qt, kt, p.N)) {
-            qb = qt;
-            ++li;
-          }
-      }
-      items[atomicAdd(&hist[hi - lo], 1)] = make_int4(kt, qa, qb, k | (n << 8) | (sbase << 16));
+      const int qa = k == 0 ? 0 : start[base + k];
+      const int qb = k == n - 1 ? T - 1 : start[base + k + 1] - 1;
+      const int w = (k + 1) * c / n - k * c / n;
+      items[atomicAdd(&hist[w], 1)] = make_int4(kt, qa, qb, k | (n << 8) | (base << 16));
     }
   }
   for (long long i = tid; i < heads * kSplitSlots; i += nth) counters[i] = 0;

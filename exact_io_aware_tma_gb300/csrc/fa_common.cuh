@@ -78,7 +78,7 @@ __device__ __forceinline__ uint32_t keep4(uint32_t w, uint32_t p8) {
 // head, planned for at most kPlanMaxTiles key tiles.
 constexpr int kSplitMax = 4;
 constexpr int kSplitSlots = 32;
-constexpr int kPlanMaxTiles = 2048;
+constexpr int kPlanMaxTiles = 1024;
 // The plan and the slots a split backward reads and writes (device
 // pointers into the caller's workspace).
 struct BwdSplit {

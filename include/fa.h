@@ -141,7 +141,7 @@ FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * Workspace for a backward call with `mask` (NULL = no mask).  With a block
- * mask (and N <= 262,144, B*H*ceil(N/128)*4 < 2^31) this adds room for
+ * mask (and N <= 131,072, B*H*ceil(N/128)*4 < 2^31) this adds room for
  * spreading the work of a key tile over up to 4 CTAs: a key tile with many
  * live query tiles (a global column, say) otherwise walks all of them in one
  * CTA while the GPU idles.  The extra part holds a work plan

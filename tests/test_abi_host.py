@@ -67,7 +67,7 @@ FAKE = 1 << 20  # an aligned non-null address; never dereferenced on reject path
 def test_masked_workspace_adds_the_split_part_only_with_a_block_mask(lib):
     # plan items (16 B x 4 per key tile), the item count, 32 counters and 32
     # fp32 slots of 2 x 128 x d per head, each part rounded to 256 bytes;
-    # nothing extra without a block mask or beyond 2048 key tiles
+    # nothing extra without a block mask or beyond 1024 key tiles
     from exact_io_aware_tma_gb300 import fa
     f = lib.fa_backward_workspace_bytes_masked
     for B, H, N, d in [(1, 8, 16384, 64), (2, 3, 300, 128), (1, 1, 1, 64)]:
@@ -81,8 +81,8 @@ def test_masked_workspace_adds_the_split_part_only_with_a_block_mask(lib):
         assert f(B, H, N, d, ctypes.byref(plain)) == base
         assert f(B, H, N, d, None) == base
     big = fa.Mask(0, -1, -1, ctypes.c_void_p(FAKE), None, 0.0, 0, 0)
-    assert f(1, 1, 2049 * 128, 64, ctypes.byref(big)) == lib.fa_backward_workspace_bytes(
-        1, 1, 2049 * 128, 64)
+    assert f(1, 1, 1025 * 128, 64, ctypes.byref(big)) == lib.fa_backward_workspace_bytes(
+        1, 1, 1025 * 128, 64)
     assert f(1, 1, 128, 96, ctypes.byref(big)) == 0
 
 
