@@ -39,6 +39,9 @@
 namespace fa {
 using namespace sm100;
 
+// Words of the per-CTA key-tile bitmask of one query tile (up to 65536 tiles).
+constexpr int kFwdLiveWords = 65536 / 32;
+
 template <int D>
 struct FwdTc {
   static constexpr int THREADS = 384;
@@ -53,7 +56,11 @@ struct FwdTc {
   static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_S = 1 + 2 * NSLOT,
                        B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  // live key tiles of the union's range under a block mask, one bit each,
+  // for query tile 0 and query tile 1
+  static constexpr int OFF_LIVE = (OFF_MISC + 64 + 127) / 128 * 128;
+  static constexpr int SMEM = OFF_LIVE + 2 * kFwdLiveWords * 4 + 1024;  // + slack for 1024-byte alignment
+  static_assert(SMEM <= 232448, "shared memory budget");
   static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
@@ -61,13 +68,27 @@ struct FwdTc {
 // Next key tile after kt that is live for query tile q0 or q1, within the
 // union's range [first, last] (the union of two adjacent tiles' ranges is one
 // range: query tile q0 + 1 starts at most one tile later than q0 ends).
-__device__ __forceinline__ int next_union_tile(const Problem& p, int q0, int q1, int klim,
-                                               int first, int last, int kt) {
+// Under a block mask the liveness comes from `live` (bit t of word block 0 /
+// 1: key tile first + t for query tile q0 / q1), built once per CTA rather
+// than read from the mask in every role's loop.
+__device__ __forceinline__ int next_union_tile(const Problem& p, const uint32_t* live, int first,
+                                               int last, int kt) {
   kt = kt + 1 < first ? first : kt + 1;
   if (p.block_mask == nullptr) return kt <= last ? kt : p.T;
-  for (; kt <= last; ++kt)
-    if (tile_live(p, q0, kt, klim) || (q1 >= 0 && tile_live(p, q1, kt, klim))) return kt;
+  while (kt <= last) {
+    const int t = kt - first;
+    const uint32_t w = (live[t >> 5] | live[kFwdLiveWords + (t >> 5)]) >> (t & 31);
+    if (w != 0) return kt + __ffs(w) - 1;  // bits past the range are 0
+    kt += 32 - (t & 31);
+  }
   return p.T;
+}
+
+// Whether key tile kt (within [first, last]) is live for query tile i of the
+// CTA, from the bitmask above.
+__device__ __forceinline__ bool live_bit(const uint32_t* live, int i, int first, int kt) {
+  const int t = kt - first;
+  return (live[i * kFwdLiveWords + (t >> 5)] >> (t & 31)) & 1u;
 }
 
 template <int D, bool PACKED, bool DROP>
@@ -133,6 +154,21 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
+  const uint32_t* live = reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE);
+  if (p.block_mask != nullptr) {
+    // liveness over the union's range, 32 key tiles per warp and word
+    const int n = ulast - ufirst + 1;
+    for (int wi = warp; wi < ((n + 31) >> 5); wi += C::THREADS / 32) {
+      const int t = (wi << 5) + lane, kt = ufirst + t;
+      const uint32_t b0 = __ballot_sync(0xffffffffu, t < n && tile_live(p, qt0, kt, klim));
+      const uint32_t b1 =
+          __ballot_sync(0xffffffffu, t < n && qt1 >= 0 && tile_live(p, qt1, kt, klim));
+      if (lane == 0) {
+        reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[wi] = b0;
+        reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[kFwdLiveWords + wi] = b1;
+      }
+    }
+  }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
@@ -158,8 +194,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
       bool ok = true;
-      for (int kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, -1); kt < p.T && ok;
-           kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, kt)) {
+      for (int kt = next_union_tile(p, live, ufirst, ulast, -1); kt < p.T && ok;
+           kt = next_union_tile(p, live, ufirst, ulast, kt)) {
         for (int which = 0; which < 2; ++which) {
           if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) {
             ok = false;
@@ -220,15 +256,15 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       // it is first_i <= kt <= last_i, so the loop needs no predicate calls.
       const bool masked = p.block_mask != nullptr;
       auto live0 = [&](int kt) {
-        return masked ? tile_live(p, qt0, kt, klim) : (kt >= first0 && kt <= last0);
+        return masked ? live_bit(live, 0, ufirst, kt) : (kt >= first0 && kt <= last0);
       };
       auto live1 = [&](int kt) {
-        return masked ? (qt1 >= 0 && tile_live(p, qt1, kt, klim)) : (kt >= first1 && kt <= last1);
+        return masked ? live_bit(live, 1, ufirst, kt) : (kt >= first1 && kt <= last1);
       };
       int slot = 0, phase = 0;  // next ring slot to consume and its phase parity
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
-      int cur = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, -1);
+      int cur = next_union_tile(p, live, ufirst, ulast, -1);
       int npv0 = 0, npv1 = 0;
       if (ok && cur < p.T) {
         ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
@@ -251,7 +287,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         const bool l1 = live1(cur);
         const int vslot = slot, vphase = phase;
         if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
-        const int nxt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, cur);
+        const int nxt = next_union_tile(p, live, ufirst, ulast, cur);
         const bool has_next = nxt < p.T;
         const bool n0 = has_next && live0(nxt);
         const bool n1 = has_next && live1(nxt);
@@ -311,9 +347,9 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       bool ok = true;
       const int myfirst = i == 0 ? first0 : first1, mylast = i == 0 ? last0 : last1;
       const bool bmask = p.block_mask != nullptr;
-      for (int kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, -1); kt < p.T;
-           kt = next_union_tile(p, qt0, qt1, klim, ufirst, ulast, kt)) {
-        if (bmask ? !tile_live(p, qt, kt, klim) : (kt < myfirst || kt > mylast)) continue;
+      for (int kt = next_union_tile(p, live, ufirst, ulast, -1); kt < p.T;
+           kt = next_union_tile(p, live, ufirst, ulast, kt)) {
+        if (bmask ? !live_bit(live, i, ufirst, kt) : (kt < myfirst || kt > mylast)) continue;
         if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
         tc_fence_after();
         float s[128];
