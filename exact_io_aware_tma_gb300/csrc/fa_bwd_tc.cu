@@ -114,6 +114,73 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
   return false;
 }
 
+// Join of a split key tile, run by the 128 element-wise threads of a part
+// (thread r owns key row r): store this part's fp32 dK, dV rows (0 if it
+// ran no step) into its slot; count the finished parts; the part that
+// finishes last adds the n slots in part order and leaves the sums in its
+// TMEM dK, dV columns for the usual epilogue.  Returns whether this CTA is
+// that part.  Kept out of line so the kernel's loops are compiled as in the
+// unsplit kernel.
+template <int D>
+__device__ __noinline__ bool split_join(const BwdSplit& sp, uint8_t* smem, uint32_t lane_base,
+                                        int r, long long bh, int meta, bool have) {
+  using C = BwdTc<D>;
+  const int nparts = (meta >> 8) & 0xff, part = meta & 0xff, sidx = meta >> 16;
+  const size_t sbase = (size_t)bh * kSplitSlots + sidx;
+  float* mine = sp.slots + ((sbase + part) * 2 * 128 + r) * D;
+  for (int t = 0; t < 2; ++t) {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (have) {
+        tmem_ld32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        reinterpret_cast<uint4*>(mine + t * 128 * D + 32 * c)[e] =
+            make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+    }
+  }
+  __threadfence();
+  named_barrier(1, 128);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 40);
+  if (r == 0) *last_flag = atomicAdd(sp.counters + sbase, 1) == nparts - 1;
+  named_barrier(1, 128);
+  const bool last = *last_flag != 0;
+  if (!last) return false;
+  __threadfence();
+  const float* slot0 = sp.slots + (sbase * 2 * 128 + r) * D;
+  for (int t = 0; t < 2; ++t) {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      float acc[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+      for (int k2 = 0; k2 < nparts; ++k2) {
+        const float4* src =
+            reinterpret_cast<const float4*>(slot0 + ((size_t)k2 * 2 * 128 + t * 128) * D + 32 * c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 x = __ldcg(src + e);
+          acc[4 * e] += x.x;
+          acc[4 * e + 1] += x.y;
+          acc[4 * e + 2] += x.z;
+          acc[4 * e + 3] += x.w;
+        }
+      }
+      uint32_t o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(acc[e]);
+      tmem_st32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
+    }
+  }
+  tmem_st_wait();
+  return true;
+}
+
 template <int D, bool PACKED, bool DROP, bool SPLIT>
 __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -458,42 +525,13 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     // Split key tile (part k of n): every part stores its fp32 dK, dV rows
     // into its own slot; the part that finishes last (a counter per key
     // tile, after a fence) sums the n slots and writes the result below.
-    int nparts = 1;
-    const float* slot0 = nullptr;
-    bool emit = true;
+    bool emit = true, have = i > 0 && ok;
     if constexpr (SPLIT) {
       // the item's part word, kept in shared memory through the loops
       const int meta = reinterpret_cast<const volatile int*>(smem + C::OFF_MISC)[11];
-      nparts = (meta >> 8) & 0xff;
-      if (nparts > 1) {
-        const int part = meta & 0xff, sidx = meta >> 16;
-        const size_t sbase = (size_t)bh * kSplitSlots + sidx;
-        float* mine = sp.slots + ((sbase + part) * 2 * 128 + r) * D;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            if (i > 0 && ok) {
-              tmem_ld32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = 0u;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              reinterpret_cast<uint4*>(mine + t * 128 * D + 32 * c)[e] =
-                  make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-          }
-        }
-        __threadfence();
-        named_barrier(1, 128);
-        volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 40);
-        if (r == 0) *last_flag = atomicAdd(sp.counters + sbase, 1) == nparts - 1;
-        named_barrier(1, 128);
-        emit = *last_flag != 0;
-        __threadfence();
-        slot0 = sp.slots + (sbase * 2 * 128 + r) * D;
+      if (((meta >> 8) & 0xff) > 1) {
+        emit = split_join<D>(sp, smem, lane_base, r, bh, meta, have);
+        have = true;
       }
     }
     uint8_t* stg = smem + C::OFF_ST;  // dK tile, then dV tile
@@ -505,26 +543,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        if (SPLIT && nparts > 1) {
-          // the parts' slots, read from L2 (written by other SMs)
-          float acc[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-          for (int k2 = 0; k2 < nparts; ++k2) {
-            const float4* src =
-                reinterpret_cast<const float4*>(slot0 + ((size_t)k2 * 2 * 128 + t * 128) * D + 32 * c);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float4 x = __ldcg(src + e);
-              acc[4 * e] += x.x;
-              acc[4 * e + 1] += x.y;
-              acc[4 * e + 2] += x.z;
-              acc[4 * e + 3] += x.w;
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(acc[e]);
-        } else if (i > 0 && ok) {
+        if (have) {
           tmem_ld32(lane_base + col + 32 * c, o);
         } else {
 #pragma unroll
