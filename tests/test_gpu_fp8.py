@@ -13,7 +13,7 @@ import torch
 from exact_io_aware_tma_gb300 import fa
 from exact_io_aware_tma_gb300.workloads import make_inputs, to_f64
 from oracle import allowed_mask, attention_forward
-from oracle.fp8 import attention_forward_fp8, dequantize
+from oracle.fp8 import attention_forward_fp8, dequantize, quantize_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +40,41 @@ def test_quantisation_bit_exact(N):
     assert np.array_equal(views["qs"].cpu().numpy().reshape(2, 2, T), qs)
     assert np.array_equal(views["ks"].cpu().numpy().reshape(2, 2, T), ks)
     assert np.array_equal(views["vs"].cpu().numpy().reshape(2, 2), vs[..., 0])
+
+
+def test_quantisation_bit_exact_every_scale_significand():
+    # The division by the block scale in the quantisation kernels: one head
+    # per bf16 significand of amax (128) at amax exponents -125 (scale below
+    # the fp32 normal range), -100, 0 and 100, each head holding amax and
+    # every bf16 value from amax * 2^-24 up to amax (both signs): every
+    # quotient's e4m3 code and every scale must equal the oracle's fp32
+    # division.
+    rng = np.random.default_rng(5)
+    heads = []
+    for e in (-125, -100, 0, 100):
+        for m in range(128):
+            amax = (1 + m / 128) * 2.0 ** e
+            vals = np.array([(1 + mm / 128) * 2.0 ** ee for ee in range(e - 24, e + 1)
+                             for mm in range(128)])
+            vals = vals[(vals <= amax) & (vals >= 2.0 ** -126)]
+            vals = np.concatenate([vals, -vals])
+            blk = np.resize(rng.permutation(vals), 128 * 128)
+            blk[rng.integers(128 * 128)] = amax
+            heads.append(blk.reshape(128, 128))
+    x = torch.from_numpy(np.stack(heads)[None]).to(torch.bfloat16)
+    H = x.shape[1]
+    assert np.array_equal(x.double().numpy(), np.stack(heads)[None])  # values are bf16
+    xd = x.cuda()
+    ws = fa.fp8_quantize(xd, xd, xd)
+    torch.cuda.synchronize()
+    views = fa.fp8_workspace_views(ws, 1, H, 128)
+    codes, scales = quantize_blocks(x.float().numpy())
+    for name, sname in (("q8", "qs"), ("k8", "ks")):
+        assert np.array_equal(e4m3_values(views[name]).reshape(1, H, 128, 128), codes), name
+        assert np.array_equal(views[sname].cpu().numpy().reshape(1, H, 1), scales), sname
+    vt = e4m3_values(views["vt8"]).reshape(1, H, 128, 128)
+    assert np.array_equal(np.swapaxes(vt, -1, -2), codes)
+    assert np.array_equal(views["vs"].cpu().numpy().reshape(1, H), scales[..., 0])
 
 
 @pytest.mark.parametrize("N,causal", [(128, False), (300, True), (1000, True), (1000, False),
