@@ -369,9 +369,12 @@ def run_gpu(args, cfg, name):
     # ---- end to end through the public API, host buffers, copies timed ----
     # Heads are independent, so the step runs over chunks of heads (each a
     # contiguous [1, hc, N, d] slice of the batch): the copy-in of a chunk,
-    # its forward + backward and its copy-out go on three streams, so copies
-    # of one chunk overlap the compute of another.  Every byte of every
-    # input and output still crosses PCIe/C2C inside the timed region.
+    # its forward + backward (on one of two compute streams, alternating, so
+    # one chunk's tail overlaps the next chunk's start) and its copy-out go
+    # on separate streams, so copies of one chunk overlap the compute of
+    # another.  Every byte of every input and output still crosses the host
+    # link inside the timed region (about 200 GB/s each way on this host,
+    # for copy engines and SM loads alike).
     e2e = None
     if not args.no_e2e:
         hq, hk, hv, hdo = (inp[x].pin_memory() for x in ("q", "k", "v", "do"))
@@ -380,6 +383,8 @@ def run_gpu(args, cfg, name):
         hc = next(c for c in (8, 4, 2, 1) if H % c == 0)
         chunks = [(b, h0, h0 + hc) for b in range(B) for h0 in range(0, H, hc)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_comp = [stream, torch.cuda.Stream(dev)]
+        ws_comp = [ws, torch.empty_like(ws)]
         e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps + 1)]
         for i in range(args.steps + 1):
@@ -399,18 +404,20 @@ def run_gpu(args, cfg, name):
                     mark(ev_qkv, s_in)
                     do[b:b + 1, h0:h1].copy_(hdo[b:b + 1, h0:h1], non_blocking=True)
                     mark(ev_do, s_in)
+            s_comp[1].wait_event(e_ev[i][0])
             for c, (b, h0, h1) in enumerate(chunks):
                 sl = (slice(b, b + 1), slice(h0, h1))
                 kvb = None if kv is None else kv[b:b + 1]
-                stream.wait_event(ev_qkv[c])
+                sc = s_comp[c % 2]
+                sc.wait_event(ev_qkv[c])
                 fa.forward(q[sl], k[sl], v[sl], causal=causal, block_mask=bm, kv_len=kvb,
-                           scale=scale, out=o[sl], lse=lse[sl])
-                mark(ev_fwd, stream)
-                stream.wait_event(ev_do[c])
+                           scale=scale, out=o[sl], lse=lse[sl], stream=sc)
+                mark(ev_fwd, sc)
+                sc.wait_event(ev_do[c])
                 fa.backward(q[sl], k[sl], v[sl], o[sl], lse[sl], do[sl], causal=causal,
-                            block_mask=bm, kv_len=kvb, scale=scale, workspace=ws, dq=dq[sl],
-                            dk=dk[sl], dv=dv[sl])
-                mark(ev_bwd, stream)
+                            block_mask=bm, kv_len=kvb, scale=scale, workspace=ws_comp[c % 2],
+                            dq=dq[sl], dk=dk[sl], dv=dv[sl], stream=sc)
+                mark(ev_bwd, sc)
             # copy-out: O and LSE once the chunk's forward is done, then the gradients
             with torch.cuda.stream(s_out):
                 for c, (b, h0, h1) in enumerate(chunks):
@@ -421,6 +428,7 @@ def run_gpu(args, cfg, name):
                     s_out.wait_event(ev_bwd[c])
                     for h_, d_ in ((hdq, dq), (hdk, dk), (hdv, dv)):
                         h_[sl].copy_(d_[sl], non_blocking=True)
+            stream.wait_stream(s_comp[1])
             stream.wait_stream(s_out)
             e_ev[i][1].record(stream)
         torch.cuda.synchronize()
@@ -429,8 +437,9 @@ def run_gpu(args, cfg, name):
         d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
         e2e = {"value": world * (f_fwd + f_bwd) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "pipeline": f"{len(chunks)} chunks of {hc} heads; copy-in, compute and "
-                           "copy-out on three streams"}
+               "pipeline": f"{len(chunks)} chunks of {hc} heads; copy-in, two alternating "
+                           "compute streams and copy-out"}
+        del ws_comp
 
     kvc = None
     if not args.no_kvcache:

@@ -244,6 +244,16 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
+    // K and V of the tile, issued by the producer thread before the rest of
+    // the set-up (TMEM, the live bitmask, the CTA barrier) so that their
+    // latency overlaps it
+    mbar_expect_tx(bar(C::B_KV), 2 * C::KT);
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_3d(s0 + C::OFF_K + h * C::HALF_K, &tm_k, bar(C::B_KV), h * 64, cy(kt * 128),
+                  cz(kt * 128));
+      tma_load_3d(s0 + C::OFF_V + h * C::HALF_K, &tm_v, bar(C::B_KV), h * 64, cy(kt * 128),
+                  cz(kt * 128));
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -280,13 +290,6 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_expect_tx(bar(C::B_KV), 2 * C::KT);
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(s0 + C::OFF_K + h * C::HALF_K, &tm_k, bar(C::B_KV), h * 64, cy(kt * 128),
-                    cz(kt * 128));
-        tma_load_3d(s0 + C::OFF_V + h * C::HALF_K, &tm_v, bar(C::B_KV), h * 64, cy(kt * 128),
-                    cz(kt * 128));
-      }
       int qt = -1, sub = 0, slot = 0, round = 0;
       while (next_q_step<D>(p, kt, klim, smem, qt, sub)) {
         const int q0 = qt * 128 + sub * 64;
@@ -578,7 +581,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
                      cz(kt * 128));
       }
       tma_store_commit();
-      tma_store_wait_all();
+      tma_store_wait_read();  // shared memory read out; the writes finish with the grid
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ

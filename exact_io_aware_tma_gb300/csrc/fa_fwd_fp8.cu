@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         for (int h = 0; h < 2; ++h)
           tma_store_3d(&tm_o, smem_u32(stage) + h * C::HALF, h * 64, qt * 128, (int)bh);
         tma_store_commit();
-        tma_store_wait_all();
+        tma_store_wait_read();  // shared memory read out; the writes finish with the grid
       }
     }
   }

@@ -149,6 +149,17 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       mbar_init(bar(i), (i == C::B_P || i == C::B_P + 1) ? 4 : 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // the query tiles, issued by the producer thread before the rest of the
+    // set-up (TMEM, the live bitmask, the CTA barrier) so that their latency
+    // overlaps it
+    mbar_expect_tx(bar(C::B_Q), (qt1 >= 0 ? 2 : 1) * C::TILE);
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_3d(s0 + C::OFF_Q + h * C::HALF, &tm_q, bar(C::B_Q), h * 64, cy(qt0 * 128),
+                  cz(qt0 * 128));
+      if (qt1 >= 0)
+        tma_load_3d(s0 + C::OFF_Q + C::TILE + h * C::HALF, &tm_q, bar(C::B_Q), h * 64,
+                    cy(qt1 * 128), cz(qt1 * 128));
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -183,14 +194,6 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_expect_tx(bar(C::B_Q), (qt1 >= 0 ? 2 : 1) * C::TILE);
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(s0 + C::OFF_Q + h * C::HALF, &tm_q, bar(C::B_Q), h * 64, cy(qt0 * 128),
-                    cz(qt0 * 128));
-        if (qt1 >= 0)
-          tma_load_3d(s0 + C::OFF_Q + C::TILE + h * C::HALF, &tm_q, bar(C::B_Q), h * 64,
-                      cy(qt1 * 128), cz(qt1 * 128));
-      }
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
       bool ok = true;
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         for (int h = 0; h < D / 64; ++h)
           tma_store_3d(&tm_o, smem_u32(stage) + h * C::HALF, h * 64, cy(qt * 128), cz(qt * 128));
         tma_store_commit();
-        tma_store_wait_all();
+        tma_store_wait_read();  // shared memory read out; the writes finish with the grid
       }
     }
   }
