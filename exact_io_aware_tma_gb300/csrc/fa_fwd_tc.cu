@@ -469,9 +469,12 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
           uint32_t o[32];
           tmem_ld32(lane_base + col_o + 32 * c, o);
           uint32_t pk[16];
+          // a row without an allowed key never had O written: 0, not stale * 0
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+            pk[j] = l > 0.f ? pack_bf16(__uint_as_float(o[2 * j]) * inv,
+                                        __uint_as_float(o[2 * j + 1]) * inv)
+                            : 0u;
           // 32 columns = four 16-byte chunks, chunk index cc = 4c + q
 #pragma unroll
           for (int q = 0; q < 4; ++q) {

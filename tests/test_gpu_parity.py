@@ -191,3 +191,23 @@ def test_invalid_arguments_on_device():
         fa.forward(q, q, q)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
     assert fa.last_device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("n,causal,kv", [(300, False, True), (300, True, False), (640, True, True),
+                                         (384, False, False)])
+def test_d64_grids_over_one_wave(n, causal, kv):
+    # d = 64 with one to four query-tile pairs per SM: odd tile counts (a
+    # pair with one tile), key lengths of 0 (pairs with no live key tile,
+    # whose O must be 0 even though its TMEM columns were never written) and
+    # short ones
+    T = (n + 127) // 128
+    B, H = 4, (200 + 4 * ((T + 1) // 2) - 1) // (4 * ((T + 1) // 2))
+    assert 152 < B * H * ((T + 1) // 2) <= 4 * 152
+    inp = make_inputs(B=B, H=H, N=n, d=64, mask="causal" if causal else "none", seed=n + H)
+    if kv:
+        inp["kv_len"] = np.array([n, 0, n // 3, 129], np.int32)
+    res = run_gpu(inp)
+    heads = [(b, h) for b in range(B) for h in range(0, H, 7)]
+    compare_heads(res, oracle_on_heads(inp, heads), heads)
+    if kv:
+        assert np.all(res["o"][1] == 0) and np.all(np.isneginf(res["lse"][1]))
