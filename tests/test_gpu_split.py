@@ -98,3 +98,29 @@ def test_split_repeats_bit_exactly():
             check_close(n, a[n], b[n], TOL_GRAD)
         else:
             assert np.array_equal(a[n], b[n]), n
+
+
+def test_three_launch_entry_points_split_like_the_one_call():
+    # fa_backward_preprocess / fa_backward_dkdv / fa_backward_dq_convert with
+    # the masked workspace (the dK/dV entry plans and splits by itself) give
+    # the one-call backward's results bit for bit in dK, dV
+    inp = make_inputs(B=1, H=3, N=2048, d=64, mask="band_global", seed=21, global_every=4)
+    g = to_device(inp)
+    B, H, N, d = g["q"].shape
+    o, lse = fa.forward(g["q"], g["k"], g["v"], block_mask=g["block_mask"], scale=g["scale"])
+    dq1, dk1, dv1 = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"],
+                                block_mask=g["block_mask"], scale=g["scale"])
+    lib, P = fa.load(), fa._ptr
+    wsb = fa.backward_workspace_bytes(B, H, N, d, g["block_mask"])
+    ws = torch.empty(wsb, device="cuda", dtype=torch.uint8)
+    dq2, dk2, dv2 = (torch.empty_like(g["q"]) for _ in range(3))
+    sp = fa._stream()
+    assert lib.fa_backward_preprocess(P(o), P(g["do"]), P(lse), B, H, N, d, P(ws), wsb, sp) == 0
+    assert lib.fa_backward_dkdv(P(g["q"]), P(g["k"]), P(g["v"]), P(g["do"]), P(dk2), P(dv2), B, H,
+                                N, d, g["scale"], 0, P(g["block_mask"]), None, P(ws), wsb,
+                                sp) == 0
+    assert lib.fa_backward_dq_convert(P(dq2), B, H, N, d, g["scale"], P(ws), wsb, sp) == 0
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    check_close("dQ", dq2.double().cpu().numpy(), dq1.double().cpu().numpy(), TOL_GRAD)
