@@ -198,7 +198,9 @@ FA_API int fa_backward_masked(const void* q, const void* k, const void* v, const
  * fa_backward_dkdv: for every live 128-key tile, recomputes P and dS from
  *   Q, K, V, dO and the workspace's LSE and D, writes dK (times scale) and
  *   dV, and adds dS K into the workspace's dQ accumulator.  Needs the
- *   preprocess first.
+ *   preprocess first.  With a block mask and a workspace of
+ *   fa_backward_workspace_bytes_masked() it is two launches (the split
+ *   plan, then the kernel).
  * fa_backward_dq_convert: dQ = scale * accumulator, rounded to bf16.
  */
 FA_API int fa_backward_preprocess(const void* o, const void* dout, const float* lse, int B,
