@@ -310,7 +310,8 @@ def run_gpu(args, cfg, name):
 
     def launch(i):
         # 4 launches of the library's kernels: fwd, preprocess, dK/dV(+dQ), dQ convert
-        # (5 with a split backward: its plan kernel runs before dK/dV)
+        # (6 with a split backward: its plan kernel runs before dK/dV, its
+        # join after)
         st = [lib.fa_forward(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, int(causal),
                              bmp, kvp, sp)]
         ev[i][1].record(stream)
@@ -472,7 +473,7 @@ def run_gpu(args, cfg, name):
                          "peak_kind": peak_kind, "traffic": traffic_record(dom)},
             "cpu_baseline": cpu_base,
             "e2e": e2e,
-            "gpu_launches": (5 if split else 4) * args.steps,
+            "gpu_launches": (6 if split else 4) * args.steps,
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "kvcache_decode": kvc,

@@ -337,14 +337,13 @@ size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
 }
 
 // Extra workspace of the split backward (block masks): the plan's items and
-// count, the slot counters and the fp32 slots; 0 where it does not apply.
+// split list (256 bytes) and the fp32 slots; 0 where it does not apply.
 static size_t split_bytes(const Problem& p) {
   const long long heads = (long long)p.B * p.H;
   if (p.block_mask == nullptr || p.T > kPlanMaxTiles ||
       heads * p.T * kSplitMax > 2147483647LL)
     return 0;
   return round_up((size_t)p.T * kSplitMax * sizeof(int4), 256) + 256 +
-         round_up((size_t)heads * kSplitSlots * sizeof(int), 256) +
          (size_t)heads * kSplitSlots * 2 * 128 * p.d * sizeof(float);
 }
 
@@ -432,8 +431,6 @@ static int backward_dkdv(const void* q, const void* k, const void* v, const void
     w += round_up((size_t)p.T * kSplitMax * sizeof(int4), 256);
     split.nitems = reinterpret_cast<const int*>(w);
     w += 256;
-    split.counters = reinterpret_cast<int*>(w);
-    w += round_up((size_t)heads * kSplitSlots * sizeof(int), 256);
     split.slots = reinterpret_cast<float*>(w);
   }
   cudaError_t e = launch_bwd_tc(p, q, k, v, dout, ws_lse2(workspace),

@@ -114,73 +114,6 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
   return false;
 }
 
-// Join of a split key tile, run by the 128 element-wise threads of a part
-// (thread r owns key row r): store this part's fp32 dK, dV rows (0 if it
-// ran no step) into its slot; count the finished parts; the part that
-// finishes last adds the n slots in part order and leaves the sums in its
-// TMEM dK, dV columns for the usual epilogue.  Returns whether this CTA is
-// that part.  Kept out of line so the kernel's loops are compiled as in the
-// unsplit kernel.
-template <int D>
-__device__ __noinline__ bool split_join(const BwdSplit& sp, uint8_t* smem, uint32_t lane_base,
-                                        int r, long long bh, int meta, bool have) {
-  using C = BwdTc<D>;
-  const int nparts = (meta >> 8) & 0xff, part = meta & 0xff, sidx = meta >> 16;
-  const size_t sbase = (size_t)bh * kSplitSlots + sidx;
-  float* mine = sp.slots + ((sbase + part) * 2 * 128 + r) * D;
-  for (int t = 0; t < 2; ++t) {
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      if (have) {
-        tmem_ld32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        reinterpret_cast<uint4*>(mine + t * 128 * D + 32 * c)[e] =
-            make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-    }
-  }
-  __threadfence();
-  named_barrier(1, 128);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 40);
-  if (r == 0) *last_flag = atomicAdd(sp.counters + sbase, 1) == nparts - 1;
-  named_barrier(1, 128);
-  const bool last = *last_flag != 0;
-  if (!last) return false;
-  __threadfence();
-  const float* slot0 = sp.slots + (sbase * 2 * 128 + r) * D;
-  for (int t = 0; t < 2; ++t) {
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      float acc[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-      for (int k2 = 0; k2 < nparts; ++k2) {
-        const float4* src =
-            reinterpret_cast<const float4*>(slot0 + ((size_t)k2 * 2 * 128 + t * 128) * D + 32 * c);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 x = __ldcg(src + e);
-          acc[4 * e] += x.x;
-          acc[4 * e + 1] += x.y;
-          acc[4 * e + 2] += x.z;
-          acc[4 * e + 3] += x.w;
-        }
-      }
-      uint32_t o[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(acc[e]);
-      tmem_st32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
-    }
-  }
-  tmem_st_wait();
-  return true;
-}
-
 template <int D, bool PACKED, bool DROP, bool SPLIT>
 __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -525,16 +458,33 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     // sequence's first rows).
     if (ok) ok = mbar_wait(bar(C::B_FIN), 0, ab);
     tc_fence_after();
-    // Split key tile (part k of n): every part stores its fp32 dK, dV rows
-    // into its own slot; the part that finishes last (a counter per key
-    // tile, after a fence) sums the n slots and writes the result below.
-    bool emit = true, have = i > 0 && ok;
+    // A part of a split key tile stores its fp32 dK, dV rows (0 if it ran no
+    // step) into its own slot; the join kernel adds the parts afterwards.
+    bool emit = true;
+    const bool have = i > 0 && ok;
     if constexpr (SPLIT) {
       // the item's part word, kept in shared memory through the loops
       const int meta = reinterpret_cast<const volatile int*>(smem + C::OFF_MISC)[11];
       if (((meta >> 8) & 0xff) > 1) {
-        emit = split_join<D>(sp, smem, lane_base, r, bh, meta, have);
-        have = true;
+        float* mine = sp.slots +
+                      (((size_t)bh * kSplitSlots + (meta >> 16) + (meta & 0xff)) * 2 * 128 + r) * D;
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            if (have) {
+              tmem_ld32(lane_base + (t == 0 ? C::COL_DK : C::COL_DV) + 32 * c, o);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<uint4*>(mine + t * 128 * D + 32 * c)[e] =
+                  make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          }
+        }
+        emit = false;
       }
     }
     uint8_t* stg = smem + C::OFF_ST;  // dK tile, then dV tile
@@ -633,10 +583,11 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
 // until the split tiles' parts fit kSplitSlots slots per head); part k
 // starts at the query tile holding live tile k*c/n, found by one warp per
 // split key tile.  Items are ordered by their number of live tiles,
-// heaviest first; the slot counters are cleared.
+// heaviest first.  plan[0] = the item count, plan[1] = the number of split
+// key tiles, then (key tile, first slot, parts) for each of them.
 __global__ void __launch_bounds__(1024)
     bwd_plan_kernel(const Problem p, int nsm, long long heads, int4* __restrict__ items,
-                    int* __restrict__ nitems, int* __restrict__ counters) {
+                    int* __restrict__ plan) {
   __shared__ int cnt[kPlanMaxTiles];
   __shared__ int meta[kPlanMaxTiles];  // n | slot base << 16
   __shared__ int hist[kPlanMaxTiles + 2];
@@ -714,7 +665,8 @@ __global__ void __launch_bounds__(1024)
       hist[w] = pos;
       pos += h;
     }
-    *nitems = pos;
+    plan[0] = pos;
+    plan[1] = nsplit;
   }
   __syncthreads();
   // items: the whole range [0, T-1] for an unsplit key tile (the kernel
@@ -728,7 +680,50 @@ __global__ void __launch_bounds__(1024)
       items[atomicAdd(&hist[w], 1)] = make_int4(kt, qa, qb, k | (n << 8) | (base << 16));
     }
   }
-  for (long long i = tid; i < heads * kSplitSlots; i += nth) counters[i] = 0;
+  for (int sk = tid; sk < nsplit; sk += nth) {
+    const int kt = split_kt[sk];
+    plan[2 + 3 * sk] = kt;
+    plan[3 + 3 * sk] = meta[kt] >> 16;
+    plan[4 + 3 * sk] = meta[kt] & 0xffff;
+  }
+}
+
+// Join of the split key tiles: block (j, bh) adds the fp32 parts of split
+// key tile j of head bh in part order, scales dK, rounds both to bf16 and
+// writes the tile's rows below N.  Eight consecutive values per thread step.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_split_join_kernel(const Problem p, long long heads, const int* __restrict__ plan,
+                          const float* __restrict__ slots, __nv_bfloat16* __restrict__ dk,
+                          __nv_bfloat16* __restrict__ dv) {
+  const int j = blockIdx.x;
+  if (j >= __ldg(plan + 1)) return;
+  const int kt = __ldg(plan + 2 + 3 * j), base = __ldg(plan + 3 + 3 * j),
+            n = __ldg(plan + 4 + 3 * j);
+  constexpr int kPart = 2 * 128 * D;  // floats of one part: dK rows, then dV rows
+  for (long long bh = blockIdx.y; bh < heads; bh += gridDim.y) {
+    const float* src = slots + ((size_t)bh * kSplitSlots + base) * kPart;
+    for (int e = threadIdx.x * 8; e < kPart; e += 256 * 8) {
+      float acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+      for (int k = 0; k < n; ++k) {
+        const float4 x0 = __ldg(reinterpret_cast<const float4*>(src + (size_t)k * kPart + e));
+        const float4 x1 = __ldg(reinterpret_cast<const float4*>(src + (size_t)k * kPart + e + 4));
+        acc[0] += x0.x, acc[1] += x0.y, acc[2] += x0.z, acc[3] += x0.w;
+        acc[4] += x1.x, acc[5] += x1.y, acc[6] += x1.z, acc[7] += x1.w;
+      }
+      const int t = e / (128 * D), r = (e / D) & 127, c = e % D;
+      const int row = kt * 128 + r;
+      if (row >= p.N) continue;
+      const float mul = t == 0 ? p.scale : 1.f;
+      const uint4 w = make_uint4(pack_bf16(acc[0] * mul, acc[1] * mul),
+                                 pack_bf16(acc[2] * mul, acc[3] * mul),
+                                 pack_bf16(acc[4] * mul, acc[5] * mul),
+                                 pack_bf16(acc[6] * mul, acc[7] * mul));
+      *reinterpret_cast<uint4*>((t == 0 ? dk : dv) + ((size_t)bh * p.N + row) * D + c) = w;
+    }
+  }
 }
 
 template <int D, bool PACKED, bool DROP, bool SPLIT>
@@ -771,7 +766,7 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
         return e;
     }
     bwd_plan_kernel<<<1, 1024, 0, st>>>(p, nsm, bh, const_cast<int4*>(split.items),
-                                        const_cast<int*>(split.nitems), split.counters);
+                                        const_cast<int*>(split.nitems));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT>;
@@ -781,6 +776,13 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
   kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad,
                                           static_cast<__nv_bfloat16*>(dk),
                                           static_cast<__nv_bfloat16*>(dv), split);
+  if constexpr (SPLIT) {
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    dim3 jgrid(kSplitSlots / 2, (unsigned)(bh < 65535 ? bh : 65535));
+    bwd_split_join_kernel<D><<<jgrid, 256, 0, st>>>(p, bh, split.nitems, split.slots,
+                                                    static_cast<__nv_bfloat16*>(dk),
+                                                    static_cast<__nv_bfloat16*>(dv));
+  }
   return cudaGetLastError();
 }
 
@@ -799,7 +801,7 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
                           void* dk, void* dv, int npad, const BwdSplit* split, cudaStream_t st) {
   const bool packed = p.cu_seqlens != nullptr, drop = p.drop_p8 != 0;
-  const BwdSplit none{nullptr, nullptr, nullptr, nullptr};
+  const BwdSplit none{nullptr, nullptr, nullptr};
   if (packed)
     return drop ? launch_bwd_tc_d<true, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
                                                      npad, none, st)

@@ -83,8 +83,9 @@ constexpr int kPlanMaxTiles = 1024;
 // pointers into the caller's workspace).
 struct BwdSplit {
   const int4* items;  // [T * kSplitMax] work items, heaviest first
-  const int* nitems;  // number of items
-  int* counters;      // [B*H][kSplitSlots] finished parts per split key tile
+  const int* nitems;  // [0]: number of items; [1]: number of split key
+                      // tiles; [2 + 3j ..]: split key tile j (tile, first
+                      // slot, parts)
   float* slots;       // [B*H][kSplitSlots][2][128][d] fp32 partial dK, dV rows
 };
 

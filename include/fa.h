@@ -145,12 +145,13 @@ FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
  * spreading the work of a key tile over up to 4 CTAs: a key tile with many
  * live query tiles (a global column, say) otherwise walks all of them in one
  * CTA while the GPU idles.  The extra part holds a work plan
- * (16 * 4 * ceil(N/128) bytes), 32 counters per head and 32 fp32 slots of
- * 2 x 128 x d values per head (1 KiB x d each), about B*H*d*32 KiB in all.  Given
- * a workspace of at least this size, fa_backward_masked / fa_backward /
+ * (16 * 4 * ceil(N/128) bytes plus 256) and 32 fp32 slots of 2 x 128 x d
+ * values per head (1 KiB x d each), about B*H*d*32 KiB in all.  Given a
+ * workspace of at least this size, fa_backward_masked / fa_backward /
  * fa_backward_dkdv launch a small planning kernel before the dK/dV kernel
- * and split heavy key tiles (each split key tile's partial dK, dV rows meet
- * in the slots and the part that finishes last writes the sum); with only
+ * and split heavy key tiles (each part of a split key tile stores its fp32
+ * dK, dV rows in its slot, and a join kernel after the dK/dV kernel adds
+ * them in part order and writes the bf16 rows); with only
  * fa_backward_workspace_bytes() they do not split.  Results agree up to the
  * order of fp32 additions.  Returns 0 for invalid sizes.
  */
@@ -199,8 +200,8 @@ FA_API int fa_backward_masked(const void* q, const void* k, const void* v, const
  *   Q, K, V, dO and the workspace's LSE and D, writes dK (times scale) and
  *   dV, and adds dS K into the workspace's dQ accumulator.  Needs the
  *   preprocess first.  With a block mask and a workspace of
- *   fa_backward_workspace_bytes_masked() it is two launches (the split
- *   plan, then the kernel).
+ *   fa_backward_workspace_bytes_masked() it is three launches (the split
+ *   plan, the kernel, the join of the split key tiles).
  * fa_backward_dq_convert: dQ = scale * accumulator, rounded to bf16.
  */
 FA_API int fa_backward_preprocess(const void* o, const void* dout, const float* lse, int B,

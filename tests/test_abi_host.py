@@ -65,16 +65,15 @@ FAKE = 1 << 20  # an aligned non-null address; never dereferenced on reject path
 
 
 def test_masked_workspace_adds_the_split_part_only_with_a_block_mask(lib):
-    # plan items (16 B x 4 per key tile), the item count, 32 counters and 32
-    # fp32 slots of 2 x 128 x d per head, each part rounded to 256 bytes;
+    # plan items (16 B x 4 per key tile), 256 bytes of counts and split list,
+    # 32 fp32 slots of 2 x 128 x d per head, each part rounded to 256 bytes;
     # nothing extra without a block mask or beyond 1024 key tiles
     from exact_io_aware_tma_gb300 import fa
     f = lib.fa_backward_workspace_bytes_masked
     for B, H, N, d in [(1, 8, 16384, 64), (2, 3, 300, 128), (1, 1, 1, 64)]:
         T = -(-N // 128)
         base = lib.fa_backward_workspace_bytes(B, H, N, d)
-        extra = (-(-T * 64 // 256) * 256 + 256 + -(-B * H * 32 * 4 // 256) * 256
-                 + B * H * 32 * 2 * 128 * d * 4)
+        extra = -(-T * 64 // 256) * 256 + 256 + B * H * 32 * 2 * 128 * d * 4
         bm = fa.Mask(0, -1, -1, ctypes.c_void_p(FAKE), None, 0.0, 0, 0)
         assert f(B, H, N, d, ctypes.byref(bm)) == base + extra
         plain = fa.Mask(1, -1, -1, None, None, 0.0, 0, 0)

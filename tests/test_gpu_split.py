@@ -1,6 +1,6 @@
 """The backward's split of heavy key tiles (block masks): a key tile whose
 column has many live query tiles is walked by several CTAs, whose partial
-dK, dV rows meet in the workspace's slots.  Checked against the oracle and
+dK, dV rows land in the workspace's slots for a join kernel to add.  Checked against the oracle and
 against the same call given only the unsplit workspace.  Marked ``gpu``."""
 
 import numpy as np
@@ -87,8 +87,8 @@ def test_split_with_dropout():
 
 
 def test_split_repeats_bit_exactly():
-    # the slot sums are added in part order by the last part to finish, so
-    # a repeated call gives the same bits whatever order the parts ran in
+    # the join adds the slots in part order, so a repeated call gives the
+    # same bits whatever order the parts ran in
     inp = make_inputs(B=1, H=4, N=2048, d=128, mask="band_global", seed=2, global_every=4)
     a, _ = run_both(inp)
     b, _ = run_both(inp)
