@@ -464,20 +464,23 @@ __global__ void __launch_bounds__(THREADS, Cfg<D, RQ>::CTAS)
       }
       __syncwarp();
       // u += p V over the warp's 16 keys; lane owns columns NC*lane .. +NC-1.
-      // Slots at or past L are skipped, not multiplied by p = 0: they may
-      // hold anything, including non-finite values.
+      // Slots at or past L are read but replaced by 0 before use (p is 0
+      // there too): they may hold anything, including non-finite values.
+      // A select rather than a loop exit lets all 16 keys' loads issue at
+      // once instead of one dependent round trip per key.
       const int nvalid = min(KPW, max(0, x.L - (t * KT + cw * KPW)));
-#pragma unroll 8
+#pragma unroll
       for (int kk = 0; kk < KPW; ++kk) {
-        if (kk >= nvalid) break;
+        const bool live = kk < nvalid;
         const int j = cw * KPW + kk;
         const float4 pv = reinterpret_cast<const float4*>(s_p)[kk];
         const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
         if constexpr (D == 128) {
           // columns 4*lane..+3: box lane/16, chunk (lane%16)/2, half lane%2
-          const uint2 w = *reinterpret_cast<const uint2*>(
+          uint2 w = *reinterpret_cast<const uint2*>(
               vb + (lane >> 4) * C::BOX + j * 128 + ((((lane & 15) >> 1) ^ (j & 7)) << 4) +
               ((lane & 1) << 3));
+          if (!live) w = make_uint2(0u, 0u);
           const float2 v0 = bf16x2_to_f2(w.x), v1 = bf16x2_to_f2(w.y);
 #pragma unroll
           for (int r = 0; r < RQ; ++r) {
@@ -486,8 +489,9 @@ __global__ void __launch_bounds__(THREADS, Cfg<D, RQ>::CTAS)
           }
         } else {
           // columns 2*lane, 2*lane+1: chunk lane/4, quarter lane%4
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(
+          uint32_t w0 = *reinterpret_cast<const uint32_t*>(
               vb + j * 128 + (((lane >> 2) ^ (j & 7)) << 4) + ((lane & 3) << 2));
+          if (!live) w0 = 0u;
           const float2 v0 = bf16x2_to_f2(w0);
 #pragma unroll
           for (int r = 0; r < RQ; ++r)
