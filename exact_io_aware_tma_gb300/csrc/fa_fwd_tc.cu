@@ -3,7 +3,9 @@
 // One CTA owns two 128-row query tiles of one (b, h) (tiles 2p and 2p+1) and
 // streams the union of their live 128-key tiles (block mask, causal rule,
 // key limit; dead tiles are never loaded) through a ring of shared-memory
-// slots filled by TMA.  The online-softmax recurrence of page
+// slots filled by TMA.  The SOLO instantiation owns one query tile (warps 2-5
+// do its softmax, TMEM columns S [0,128), O [128,128+d)) and runs two CTAs
+// per SM.  The online-softmax recurrence of page
 // "FlashAttention" (aiwiki), section "Tiling and online normalization", is
 // evaluated per query row in log2 units with a lazily moved reference:
 //     m' = max over the tile of scale*log2(e)*q.k_j
@@ -42,14 +44,21 @@ using namespace sm100;
 // Words of the per-CTA key-tile bitmask of one query tile (up to 65536 tiles).
 constexpr int kFwdLiveWords = 65536 / 32;
 
-template <int D>
+// SOLO: one query tile per CTA (192 threads: producer, MMA issuer, four
+// softmax warps; 256 TMEM columns; a shallower ring) so that two CTAs share
+// an SM -- for short sequences, where a CTA's fixed costs (set-up, first
+// tile, epilogue) are a large part of its time and two CTAs hide each
+// other's.
+template <int D, bool SOLO = false>
 struct FwdTc {
-  static constexpr int THREADS = 384;
-  static constexpr int NSLOT = D == 64 ? 8 : 4;  // K/V ring slots
+  static constexpr int THREADS = SOLO ? 192 : 384;
+  static constexpr int WARP_SM = SOLO ? 2 : 4;   // first softmax warp
+  static constexpr int NQ = SOLO ? 1 : 2;        // query tiles per CTA
+  static constexpr int NSLOT = SOLO ? (D == 64 ? 4 : 2) : (D == 64 ? 8 : 4);  // K/V ring slots
   static constexpr int HALF = 128 * 128;         // one 128-row x 64-col bf16 box
   static constexpr int TILE = 128 * D * 2;       // one 128-row tile
   static constexpr int OFF_Q = 0;                // Q0, Q1 (reused for O staging)
-  static constexpr int OFF_KV = 2 * TILE;
+  static constexpr int OFF_KV = NQ * TILE;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
   // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_ready[2],
   // o_done[2], drain
@@ -59,10 +68,10 @@ struct FwdTc {
   // live key tiles of the union's range under a block mask, one bit each,
   // for query tile 0 and query tile 1
   static constexpr int OFF_LIVE = (OFF_MISC + 64 + 127) / 128 * 128;
-  static constexpr int SMEM = OFF_LIVE + 2 * kFwdLiveWords * 4 + 1024;  // + slack for 1024-byte alignment
-  static_assert(SMEM <= 232448, "shared memory budget");
-  static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
-  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int SMEM = OFF_LIVE + NQ * kFwdLiveWords * 4 + 1024;  // + slack for 1024-byte alignment
+  static_assert(SMEM <= (SOLO ? 232448 / 2 - 1024 : 232448), "shared memory budget");
+  static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = SOLO ? 128 : 256, COL_O1 = 256 + D;
+  static constexpr uint32_t TMEM_COLS = SOLO ? 256 : 512;
 };
 
 // Next key tile after kt that is live for query tile q0 or q1, within the
@@ -71,13 +80,15 @@ struct FwdTc {
 // Under a block mask the liveness comes from `live` (bit t of word block 0 /
 // 1: key tile first + t for query tile q0 / q1), built once per CTA rather
 // than read from the mask in every role's loop.
+template <bool SOLO = false>
 __device__ __forceinline__ int next_union_tile(const Problem& p, const uint32_t* live, int first,
                                                int last, int kt) {
   kt = kt + 1 < first ? first : kt + 1;
   if (p.block_mask == nullptr) return kt <= last ? kt : p.T;
   while (kt <= last) {
     const int t = kt - first;
-    const uint32_t w = (live[t >> 5] | live[kFwdLiveWords + (t >> 5)]) >> (t & 31);
+    const uint32_t w =
+        (live[t >> 5] | (SOLO ? 0u : live[kFwdLiveWords + (t >> 5)])) >> (t & 31);
     if (w != 0) return kt + __ffs(w) - 1;  // bits past the range are 0
     kt += 32 - (t & 31);
   }
@@ -91,18 +102,19 @@ __device__ __forceinline__ bool live_bit(const uint32_t* live, int i, int first,
   return (live[i * kFwdLiveWords + (t >> 5)] >> (t & 31)) & 1u;
 }
 
-template <int D, bool PACKED, bool DROP>
-__global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
+template <int D, bool PACKED, bool DROP, bool SOLO>
+__global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const Problem pin, float* __restrict__ lse, __nv_bfloat16* __restrict__ o_rows) {
-  using C = FwdTc<D>;
+  using C = FwdTc<D, SOLO>;
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
   // (coordinates (x, h, start + row)), whose length then plays the role of N.
   // Grid: one CTA per (head, query-tile pair) in the grouped order
-  // (heaviest pairs first across a group of heads whose K and V stay in L2).
-  const int npairs_grid = (pin.T + 1) / 2;
+  // (heaviest pairs first across a group of heads whose K and V stay in L2);
+  // SOLO: one CTA per (head, query tile), in the same order.
+  const int npairs_grid = SOLO ? pin.T : (pin.T + 1) / 2;
   long long bh;
   int yi;
   grouped_cta(pin, blockIdx.x, npairs_grid, bh, yi);
@@ -116,7 +128,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
     p.N = len;
     p.T = (len + kTile - 1) / kTile;
   }
-  const int npairs = (p.T + 1) / 2;
+  const int npairs = SOLO ? p.T : (p.T + 1) / 2;
   if (yi >= npairs) return;  // packed: past this sequence's tiles
   auto cy = [&](int row) { return PACKED ? head : row; };
   auto cz = [&](int row) { return PACKED ? start + row : (int)bh; };
@@ -133,8 +145,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = npairs - 1 - yi;  // heaviest causal pairs first
-  const int qt0 = 2 * pair;
-  const int qt1 = (2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
+  const int qt0 = SOLO ? pair : 2 * pair;
+  const int qt1 = (!SOLO && 2 * pair + 1 < p.T) ? 2 * pair + 1 : -1;
   const int klim = key_limit(p, b);
   // Live key tiles of each query tile (exact without a block mask, a bound
   // with one) and of their union.
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
           __ballot_sync(0xffffffffu, t < n && qt1 >= 0 && tile_live(p, qt1, kt, klim));
       if (lane == 0) {
         reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[wi] = b0;
-        reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[kFwdLiveWords + wi] = b1;
+        if constexpr (!SOLO) reinterpret_cast<uint32_t*>(smem + C::OFF_LIVE)[kFwdLiveWords + wi] = b1;
       }
     }
   }
@@ -197,8 +209,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
       bool ok = true;
-      for (int kt = next_union_tile(p, live, ufirst, ulast, -1); kt < p.T && ok;
-           kt = next_union_tile(p, live, ufirst, ulast, kt)) {
+      for (int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1); kt < p.T && ok;
+           kt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt)) {
         for (int which = 0; which < 2; ++which) {
           if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) {
             ok = false;
@@ -262,12 +274,13 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         return masked ? live_bit(live, 0, ufirst, kt) : (kt >= first0 && kt <= last0);
       };
       auto live1 = [&](int kt) {
+        if constexpr (SOLO) return false;
         return masked ? live_bit(live, 1, ufirst, kt) : (kt >= first1 && kt <= last1);
       };
       int slot = 0, phase = 0;  // next ring slot to consume and its phase parity
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
-      int cur = next_union_tile(p, live, ufirst, ulast, -1);
+      int cur = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
       int npv0 = 0, npv1 = 0;
       if (ok && cur < p.T) {
         ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
@@ -290,7 +303,7 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
         const bool l1 = live1(cur);
         const int vslot = slot, vphase = phase;
         if (++slot == C::NSLOT) { slot = 0; phase ^= 1; }
-        const int nxt = next_union_tile(p, live, ufirst, ulast, cur);
+        const int nxt = next_union_tile<SOLO>(p, live, ufirst, ulast, cur);
         const bool has_next = nxt < p.T;
         const bool n0 = has_next && live0(nxt);
         const bool n1 = has_next && live1(nxt);
@@ -334,9 +347,9 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= C::WARP_SM) {
     // ------------------------------------------------------------ softmax
-    const int i = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int i = (warp - C::WARP_SM) >> 2;  // query tile of this warpgroup
     const int qt = i == 0 ? qt0 : qt1;
     if (qt >= 0) {
       const int r = ((warp & 3) << 5) + lane;  // row within the tile = TMEM lane
@@ -350,8 +363,8 @@ __global__ void __launch_bounds__(FwdTc<D>::THREADS, 1)
       bool ok = true;
       const int myfirst = i == 0 ? first0 : first1, mylast = i == 0 ? last0 : last1;
       const bool bmask = p.block_mask != nullptr;
-      for (int kt = next_union_tile(p, live, ufirst, ulast, -1); kt < p.T;
-           kt = next_union_tile(p, live, ufirst, ulast, kt)) {
+      for (int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1); kt < p.T;
+           kt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt)) {
         if (bmask ? !live_bit(live, i, ufirst, kt) : (kt < myfirst || kt > mylast)) continue;
         if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
         tc_fence_after();
@@ -520,10 +533,10 @@ static int heads_per_group(long long heads, long long bytes_per_head) {
   return (int)g;
 }
 
-template <int D, bool PACKED, bool DROP>
+template <int D, bool PACKED, bool DROP, bool SOLO>
 static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void* k,
                                    const void* v, void* o, float* lse, cudaStream_t st) {
-  using C = FwdTc<D>;
+  using C = FwdTc<D, SOLO>;
   Problem p = pin;
   p.hgroup = heads_per_group((long long)p.B * p.H, (long long)p.N * D * 4);
   const long long bh = (long long)p.B * p.H;
@@ -538,11 +551,11 @@ static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void
     maps = make_bf16_map_3d(&tq, q, D, p.N, bh, 128) && make_bf16_map_3d(&tk, k, D, p.N, bh, 128) &&
            make_bf16_map_3d(&tv, v, D, p.N, bh, 128) && make_bf16_map_3d(&to, o, D, p.N, bh, 128);
   if (!maps) return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D, PACKED, DROP>;
+  auto kern = fwd_tc_kernel<D, PACKED, DROP, SOLO>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(bh * ((p.T + 1) / 2)));
+  dim3 grid((unsigned)(bh * (SOLO ? p.T : (p.T + 1) / 2)));
   kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, to, p, lse,
                                           static_cast<__nv_bfloat16*>(o));
   return cudaGetLastError();
@@ -551,8 +564,22 @@ static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void
 template <bool PACKED, bool DROP>
 static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
                                    void* o, float* lse, cudaStream_t st) {
-  return p.d == 64 ? launch_fwd_tc_t<64, PACKED, DROP>(p, q, k, v, o, lse, st)
-                   : launch_fwd_tc_t<128, PACKED, DROP>(p, q, k, v, o, lse, st);
+  return p.d == 64 ? launch_fwd_tc_t<64, PACKED, DROP, false>(p, q, k, v, o, lse, st)
+                   : launch_fwd_tc_t<128, PACKED, DROP, false>(p, q, k, v, o, lse, st);
+}
+
+// One query tile per CTA, two CTAs per SM (padded layout, no dropout): at
+// d = 64, where a tile pair's fixed costs weigh most against its short MMAs
+// (measured 1.01-1.10x on causal and full masks of N = 1024-8192, 1.2x on a
+// band-plus-global block mask), and at d = 128 under a sliding window
+// narrower than 2048 keys on each side (1.07x at a 1024-key causal window);
+// other d = 128 work runs faster as pairs, which share each K/V tile between
+// two query tiles (0.87x-1.0x as SOLO).
+static bool use_solo(const Problem& p) {
+  if (p.d == 64) return true;
+  const bool narrow_left = p.wl >= 0 && p.wl < 2048;
+  const bool narrow_right = p.causal || (p.wr >= 0 && p.wr < 2048);
+  return narrow_left && narrow_right;
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* o,
@@ -561,6 +588,9 @@ cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const 
   if (packed)
     return drop ? launch_fwd_tc_d<true, true>(p, q, k, v, o, lse, st)
                 : launch_fwd_tc_d<true, false>(p, q, k, v, o, lse, st);
+  if (!drop && use_solo(p))
+    return p.d == 64 ? launch_fwd_tc_t<64, false, false, true>(p, q, k, v, o, lse, st)
+                     : launch_fwd_tc_t<128, false, false, true>(p, q, k, v, o, lse, st);
   return drop ? launch_fwd_tc_d<false, true>(p, q, k, v, o, lse, st)
               : launch_fwd_tc_d<false, false>(p, q, k, v, o, lse, st);
 }
