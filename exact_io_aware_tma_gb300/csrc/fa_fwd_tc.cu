@@ -561,25 +561,35 @@ static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void
   return cudaGetLastError();
 }
 
-template <bool PACKED, bool DROP>
-static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
-                                   void* o, float* lse, cudaStream_t st) {
-  return p.d == 64 ? launch_fwd_tc_t<64, PACKED, DROP, false>(p, q, k, v, o, lse, st)
-                   : launch_fwd_tc_t<128, PACKED, DROP, false>(p, q, k, v, o, lse, st);
-}
-
-// One query tile per CTA, two CTAs per SM (padded layout, no dropout): at
-// d = 64, where a tile pair's fixed costs weigh most against its short MMAs
-// (measured 1.01-1.10x on causal and full masks of N = 1024-8192, 1.2x on a
-// band-plus-global block mask), and at d = 128 under a sliding window
-// narrower than 2048 keys on each side (1.07x at a 1024-key causal window);
-// other d = 128 work runs faster as pairs, which share each K/V tile between
-// two query tiles (0.87x-1.0x as SOLO).
+// One query tile per CTA, two CTAs per SM, where it measured faster than
+// the tile pair (same bits out):
+//  - d = 64, padded, no dropout: always (1.01-1.10x on causal and full masks
+//    of N = 1024-8192, 1.2x on a band-plus-global block mask), since a
+//    pair's fixed costs weigh most against its short MMAs;
+//  - d = 64 with dropout or packed sequences: up to 2048 rows (1.12x with
+//    dropout at N = 1024, 1.04x for 16 sequences of 512-2048), not beyond
+//    (0.95x with dropout at N = 8192, 0.93x for sequences up to 8192);
+//  - d = 128 (padded, no dropout): only under a sliding window narrower than
+//    2048 keys on each side (1.07x at a 1024-key causal window); other
+//    d = 128 work runs faster as pairs, which share each K/V tile between
+//    two query tiles (0.87x-1.0x as one-tile CTAs).
 static bool use_solo(const Problem& p) {
-  if (p.d == 64) return true;
+  if (p.d == 64) return (p.drop_p8 == 0 && p.cu_seqlens == nullptr) || p.N <= 2048;
+  if (p.cu_seqlens != nullptr || p.drop_p8 != 0) return false;
   const bool narrow_left = p.wl >= 0 && p.wl < 2048;
   const bool narrow_right = p.causal || (p.wr >= 0 && p.wr < 2048);
   return narrow_left && narrow_right;
+}
+
+template <bool PACKED, bool DROP>
+static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
+                                   void* o, float* lse, cudaStream_t st) {
+  if (p.d == 64)
+    return use_solo(p) ? launch_fwd_tc_t<64, PACKED, DROP, true>(p, q, k, v, o, lse, st)
+                       : launch_fwd_tc_t<64, PACKED, DROP, false>(p, q, k, v, o, lse, st);
+  if constexpr (!PACKED && !DROP)
+    if (use_solo(p)) return launch_fwd_tc_t<128, false, false, true>(p, q, k, v, o, lse, st);
+  return launch_fwd_tc_t<128, PACKED, DROP, false>(p, q, k, v, o, lse, st);
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* o,
@@ -588,9 +598,6 @@ cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const 
   if (packed)
     return drop ? launch_fwd_tc_d<true, true>(p, q, k, v, o, lse, st)
                 : launch_fwd_tc_d<true, false>(p, q, k, v, o, lse, st);
-  if (!drop && use_solo(p))
-    return p.d == 64 ? launch_fwd_tc_t<64, false, false, true>(p, q, k, v, o, lse, st)
-                     : launch_fwd_tc_t<128, false, false, true>(p, q, k, v, o, lse, st);
   return drop ? launch_fwd_tc_d<false, true>(p, q, k, v, o, lse, st)
               : launch_fwd_tc_d<false, false>(p, q, k, v, o, lse, st);
 }
