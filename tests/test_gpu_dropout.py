@@ -132,3 +132,13 @@ def test_dropout_probability_is_validated():
         with pytest.raises(fa.FAError) as e:
             fa.forward(q, q, q, dropout=(p, 0, 0))
         assert e.value.status == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n", [2048, 2176])
+def test_dropout_d64_on_both_sides_of_the_cta_shape_threshold(n):
+    # at d = 64 with dropout the forward runs one query tile per CTA up to
+    # 2048 rows and a pair of query tiles per CTA beyond: both match
+    inp = make_inputs(B=1, H=1, N=n, d=64, mask="causal", seed=n)
+    inp["dropout"] = dict(p=0.15, seed=4242, offset=7)
+    heads = [(0, 0)]
+    compare_heads(run_gpu(inp), oracle_on_heads(inp, heads), heads)

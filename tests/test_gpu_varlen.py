@@ -69,3 +69,10 @@ def test_bad_offsets_are_reported_not_faulted():
     torch.cuda.synchronize()
     assert fa.last_device_status() == fa.FA_ERR_INVALID_ARG
     assert fa.last_device_status() == fa.FA_OK  # the word is cleared by the read
+
+
+@pytest.mark.parametrize("lens", [[2048, 300], [2100, 1, 300]])
+def test_packed_d64_on_both_sides_of_the_cta_shape_threshold(lens):
+    # at d = 64 packed sequences run one query tile per CTA while the
+    # longest is at most 2048 rows, a pair of query tiles per CTA beyond
+    run(lens, 2, 64, causal=True, seed=len(lens))
