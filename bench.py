@@ -381,7 +381,7 @@ def run_gpu(args, cfg, name):
         hq, hk, hv, hdo = (inp[x].pin_memory() for x in ("q", "k", "v", "do"))
         ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
         hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        hc = next(c for c in (8, 4, 2, 1) if H % c == 0)
+        hc = next(c for c in range(min(args.e2e_chunk_heads, H), 0, -1) if H % c == 0)
         chunks = [(b, h0, h0 + hc) for b in range(B) for h0 in range(0, H, hc)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         s_comp = [stream, torch.cuda.Stream(dev)]
@@ -863,6 +863,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kvcache", action="store_true",
                     help="skip the KV-cache decode figure of the default line")
+    ap.add_argument("--e2e-chunk-heads", type=int, default=8,
+                    help="heads per chunk of the end-to-end pipeline (largest divisor of H "
+                         "not above this)")
     args = ap.parse_args()
     if args.workload in MASK_WORKLOADS:
         if args.impl == "reference":
