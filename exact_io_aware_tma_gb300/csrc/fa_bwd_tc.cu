@@ -64,8 +64,8 @@ struct BwdTc {
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
                        B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  // misc: TMEM address (+0), abort flag (+16), last-part flag (+40) and the
-  // split item's part word (+44)
+  // misc: TMEM address (+0), abort flag (+16) and the split item's part
+  // word (+44)
   // dropout keep bytes of a step, [64 queries][128 keys], two buffers
   static constexpr int OFF_DROP = (OFF_MISC + 64 + 127) / 128 * 128;
   static constexpr int DROPB = BQ * 128;
