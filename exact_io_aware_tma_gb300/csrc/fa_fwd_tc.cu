@@ -584,9 +584,15 @@ static bool use_solo(const Problem& p) {
 template <bool PACKED, bool DROP>
 static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
                                    void* o, float* lse, cudaStream_t st) {
-  if (p.d == 64)
-    return use_solo(p) ? launch_fwd_tc_t<64, PACKED, DROP, true>(p, q, k, v, o, lse, st)
-                       : launch_fwd_tc_t<64, PACKED, DROP, false>(p, q, k, v, o, lse, st);
+  if (p.d == 64) {
+    // padded without dropout use_solo() always holds at d = 64: no pair
+    // instantiation is built for it
+    if constexpr (!PACKED && !DROP)
+      return launch_fwd_tc_t<64, false, false, true>(p, q, k, v, o, lse, st);
+    else
+      return use_solo(p) ? launch_fwd_tc_t<64, PACKED, DROP, true>(p, q, k, v, o, lse, st)
+                         : launch_fwd_tc_t<64, PACKED, DROP, false>(p, q, k, v, o, lse, st);
+  }
   if constexpr (!PACKED && !DROP)
     if (use_solo(p)) return launch_fwd_tc_t<128, false, false, true>(p, q, k, v, o, lse, st);
   return launch_fwd_tc_t<128, PACKED, DROP, false>(p, q, k, v, o, lse, st);
