@@ -53,9 +53,36 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# Datasheet dense-BF16 tensor peak of one GB300 (Blackwell Ultra) GPU:
+# NVIDIA's GB300 NVL72 specification lists 360 PFLOPS of FP16/BF16 tensor
+# throughput with 2:4 sparsity for 72 GPUs, i.e. 5 PFLOP/s sparse and
+# 2.5 PFLOP/s dense per GPU.  (152 SMs x 8192 dense bf16 FLOP per clock per
+# SM x 2.07 GHz, the maximum SM clock, gives 2.58 PFLOP/s.)
+DATASHEET_BF16_TFLOPS = 2500.0
+DATASHEET_SOURCE = ("NVIDIA GB300 NVL72 specification: 360 PFLOPS FP16/BF16 with sparsity "
+                    "over 72 GPUs -> 2.5 PFLOP/s dense per GPU")
+
+
 def flops(cfg, dense_fraction):
     fwd = 4.0 * cfg["B"] * cfg["H"] * cfg["N"] ** 2 * cfg["d"] * dense_fraction
     return fwd, 2.5 * fwd
+
+
+def effective_fraction(cfg, inp):
+    """Fraction of the dense N^2 pairs a key-padding mask leaves: the mean of
+    kv_len[b] / N over the batch (sum_b N*kv_len[b] over B*N^2).  None for
+    other masks (their metric count is already exact up to the diagonal)."""
+    if inp.get("kv_len") is None:
+        return None
+    N = cfg["N"]
+    return float(sum(min(max(int(x), 0), N) for x in inp["kv_len"])) / (len(inp["kv_len"]) * N)
+
+
+def workload_config(name, cfg, world):
+    """The `config` object of a line, the same for both arms."""
+    return {"workload": name, **{k: cfg[k] for k in ("B", "H", "N", "d", "mask")},
+            "parallelism": f"replicas{world}",
+            "l2": "GPU arm: flushed between steps (256 MB write)"}
 
 
 def dense_fraction(cfg):
@@ -202,7 +229,7 @@ def run_reference(args, cfg, name):
         "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
         "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, **{k: cfg[k] for k in ("B", "H", "N", "d", "mask")}},
+        "config": workload_config(name, cfg, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -263,6 +290,135 @@ def traffic_record(kernel):
     return float(r["bytes_per_launch_full"])
 
 
+class Step:
+    """Device-resident inputs, outputs and workspace of one workload and the
+    launch sequence of one step through the C ABI: forward, backward
+    preprocess, dK/dV (+dQ accumulation), dQ conversion -- 4 launches of the
+    library's kernels (6 when a block-masked backward splits heavy key
+    tiles: its plan kernel runs before dK/dV and its join after)."""
+
+    def __init__(self, cfg, inp, dev, stream):
+        import torch
+        from exact_io_aware_tma_gb300 import fa
+        self.lib = fa.load()
+        B, H, N, d = cfg["B"], cfg["H"], cfg["N"], cfg["d"]
+        self.shape = (B, H, N, d)
+        self.causal = int(inp["causal"])
+        self.scale = inp["scale"]
+        self.bm = None if inp["block_mask"] is None else torch.from_numpy(inp["block_mask"]).to(dev)
+        self.kv = None if inp["kv_len"] is None else torch.from_numpy(inp["kv_len"]).to(dev)
+        t = {x: inp[x].to(dev) for x in ("q", "k", "v", "do")}
+        t["o"] = torch.empty_like(t["q"])
+        t["lse"] = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        for x in ("dq", "dk", "dv"):
+            t[x] = torch.empty_like(t["q"])
+        self.t = t
+        # with a block mask, room for the backward's split of heavy key tiles
+        self.wsb = fa.backward_workspace_bytes(B, H, N, d, self.bm)
+        self.split = self.wsb > fa.backward_workspace_bytes(B, H, N, d)
+        self.ws = torch.empty(self.wsb, device=dev, dtype=torch.uint8)
+        self.stream = stream
+        self.launches = 6 if self.split else 4
+
+    def launch(self, ev):
+        """One step; ev[1], ev[2], ev[3] are recorded after the forward, the
+        preprocess and the dK/dV call (ev[0] / ev[4] belong to the caller)."""
+        from exact_io_aware_tma_gb300 import fa
+        lib, P, t, st_ = self.lib, fa._ptr, self.t, self.stream
+        sp = fa._stream(st_)
+        B, H, N, d = self.shape
+        bmp, kvp, ws, wsb = P(self.bm), P(self.kv), P(self.ws), self.wsb
+        st = [lib.fa_forward(P(t["q"]), P(t["k"]), P(t["v"]), P(t["o"]), P(t["lse"]), B, H, N,
+                             d, self.scale, self.causal, bmp, kvp, sp)]
+        ev[1].record(st_)
+        st.append(lib.fa_backward_preprocess(P(t["o"]), P(t["do"]), P(t["lse"]), B, H, N, d, ws,
+                                             wsb, sp))
+        ev[2].record(st_)
+        st.append(lib.fa_backward_dkdv(P(t["q"]), P(t["k"]), P(t["v"]), P(t["do"]), P(t["dk"]),
+                                       P(t["dv"]), B, H, N, d, self.scale, self.causal, bmp, kvp,
+                                       ws, wsb, sp))
+        ev[3].record(st_)
+        st.append(lib.fa_backward_dq_convert(P(t["dq"]), B, H, N, d, self.scale, ws, wsb, sp))
+        if any(s != 0 for s in st):
+            raise RuntimeError(f"library call failed: {[fa.status_string(s) for s in st]}")
+
+
+def time_workload_table(steps, warmup, dev, flush, min_seconds=0.4):
+    """Forward and backward TFLOP/s of every workload of the method's list
+    (tiny, BERT key padding, GPT-2 causal, long-context causal, block
+    sparse), each timed like the headline step: L2 flushed before every step
+    (outside the events), CUDA events around each launch on the launching
+    stream.  A workload runs at least `steps` timed steps and keeps going
+    (in rounds of `steps`) until `min_seconds` of wall time have passed, so
+    the SM clock sampler sees it under load; every timed step counts."""
+    import numpy as np
+    import torch
+    from exact_io_aware_tma_gb300 import fa
+    from exact_io_aware_tma_gb300.workloads import WORKLOADS, make_inputs
+    peak, peak_kind = peaks()
+    stream = torch.cuda.current_stream(dev)
+    table = {}
+    for name, cfg in WORKLOADS.items():
+        inp = make_inputs(**cfg)
+        step = Step(cfg, inp, dev, stream)
+        for _ in range(max(3, warmup)):
+            flush.zero_()
+            step.launch([torch.cuda.Event(enable_timing=True) for _ in range(5)])
+        torch.cuda.synchronize()
+        segs, n = [], 0
+        with ClockSampler(dev.index or 0) as clk:
+            time.sleep(0.3)
+            t0 = time.perf_counter()
+            while n < steps or time.perf_counter() - t0 < min_seconds:
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+                       for _ in range(steps)]
+                for ev in evs:
+                    flush.zero_()
+                    ev[0].record(stream)
+                    step.launch(ev)
+                    ev[4].record(stream)
+                torch.cuda.synchronize()
+                segs += [[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in evs]
+                n += steps
+        if fa.last_device_status(stream) != 0:
+            raise RuntimeError(f"{name}: device status not OK")
+        seg = np.array(segs)
+        fwd_ms = float(seg[:, 0].mean())
+        bwd_ms = float(seg[:, 1:].sum(axis=1).mean())
+        f_fwd, f_bwd = flops(cfg, dense_fraction(cfg))
+        fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+        bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+        row = {
+            "B": cfg["B"], "H": cfg["H"], "N": cfg["N"], "d": cfg["d"], "mask": cfg["mask"],
+            "fwd_gflop": f_fwd / 1e9, "bwd_gflop": f_bwd / 1e9,
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "bwd_kernel_ms": {"preprocess": float(seg[:, 1].mean()),
+                              "dkdv": float(seg[:, 2].mean()),
+                              "dq_convert": float(seg[:, 3].mean())},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "pct_of_measured_peak": {"fwd": 100 * fwd_tf / peak, "bwd": 100 * bwd_tf / peak},
+            "pct_of_datasheet_peak": {"fwd": 100 * fwd_tf / DATASHEET_BF16_TFLOPS,
+                                      "bwd": 100 * bwd_tf / DATASHEET_BF16_TFLOPS},
+            "timed_steps": n, "launches_per_step": step.launches,
+            "clocks": clk.summary(),
+        }
+        eff = effective_fraction(cfg, inp)
+        if eff is not None:
+            # key padding: the metric credits the dense N^2 pairs; the
+            # effective figure counts only the sum_b N*kv_len[b] unmasked ones
+            row["effective"] = {"pair_fraction": eff, "fwd_tflops": fwd_tf * eff,
+                                "bwd_tflops": bwd_tf * eff,
+                                "note": "FLOPs over sum_b N*kv_len[b] unmasked pairs only"}
+        table[name] = row
+        del step
+        torch.cuda.empty_cache()
+    return {"peaks": {"measured_tflops": peak, "measured_kind": peak_kind,
+                      "datasheet_tflops": DATASHEET_BF16_TFLOPS,
+                      "datasheet_source": DATASHEET_SOURCE},
+            "l2": "flushed before every step (256 MB write, outside the events)",
+            "rows": table}
+
+
 def run_gpu(args, cfg, name):
     import numpy as np
     import torch
@@ -292,37 +448,15 @@ def run_gpu(args, cfg, name):
     causal = inp["causal"]
     bm = None if inp["block_mask"] is None else torch.from_numpy(inp["block_mask"]).to(dev)
     kv = None if inp["kv_len"] is None else torch.from_numpy(inp["kv_len"]).to(dev)
-    q, k, v, do = (inp[x].to(dev) for x in ("q", "k", "v", "do"))
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    # with a block mask, room for the backward's split of heavy key tiles
-    wsb = fa.backward_workspace_bytes(B, H, N, d, bm)
-    split = wsb > fa.backward_workspace_bytes(B, H, N, d)
-    ws = torch.empty(wsb, device=dev, dtype=torch.uint8)
-    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)  # > 129 MB L2
-    lib = fa.load()
     stream = torch.cuda.current_stream(dev)
-    sp = fa._stream(stream)
-    P = fa._ptr
-    scale = inp["scale"]
-    bmp, kvp = P(bm), P(kv)
+    step = Step(cfg, inp, dev, stream)
+    q, k, v, do, o, lse, dq, dk, dv = (step.t[x] for x in ("q", "k", "v", "do", "o", "lse",
+                                                            "dq", "dk", "dv"))
+    ws, split, scale = step.ws, step.split, inp["scale"]
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)  # > 129 MB L2
 
     def launch(i):
-        # 4 launches of the library's kernels: fwd, preprocess, dK/dV(+dQ), dQ convert
-        # (6 with a split backward: its plan kernel runs before dK/dV, its
-        # join after)
-        st = [lib.fa_forward(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, int(causal),
-                             bmp, kvp, sp)]
-        ev[i][1].record(stream)
-        st.append(lib.fa_backward_preprocess(P(o), P(do), P(lse), B, H, N, d, P(ws), wsb, sp))
-        ev[i][2].record(stream)
-        st.append(lib.fa_backward_dkdv(P(q), P(k), P(v), P(do), P(dk), P(dv), B, H,
-                                       N, d, scale, int(causal), bmp, kvp, P(ws), wsb, sp))
-        ev[i][3].record(stream)
-        st.append(lib.fa_backward_dq_convert(P(dq), B, H, N, d, scale, P(ws), wsb, sp))
-        if any(s != 0 for s in st):
-            raise RuntimeError(f"library call failed: {[fa.status_string(s) for s in st]}")
+        step.launch(ev[i])
 
     n_ev = max(args.warmup, args.steps)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_ev)]
@@ -366,6 +500,11 @@ def run_gpu(args, cfg, name):
     kernels = {"fwd": (f_fwd, fwd_ms), "bwd_dkdv": (f_bwd, dkdv_ms)}
     dom = max(kernels, key=lambda n: kernels[n][1])
     achieved = kernels[dom][0] / (kernels[dom][1] * 1e-3) / 1e12
+
+    # ---- every workload of the method's list, timed the same way ----
+    table = None
+    if not args.no_workloads:
+        table = time_workload_table(args.steps, args.warmup, dev, flush)
 
     # ---- end to end through the public API, host buffers, copies timed ----
     # Heads are independent, so the step runs over chunks of heads (each a
@@ -458,14 +597,16 @@ def run_gpu(args, cfg, name):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": name, "B": B, "H": H, "N": N, "d": d,
-                       "mask": cfg["mask"], "parallelism": f"replicas{world}",
-                       "l2": "flushed between steps (256 MB write)"},
+            "config": workload_config(name, cfg, world),
             "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
             "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
             "pct_of_peak": {"fwd": 100 * f_fwd / (fwd_ms * 1e-3) / 1e12 / peak,
                             "bwd": 100 * f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,
                             "peak_tflops": peak, "peak_kind": peak_kind},
+            "pct_of_datasheet_peak": {
+                "fwd": 100 * f_fwd / (fwd_ms * 1e-3) / 1e12 / DATASHEET_BF16_TFLOPS,
+                "bwd": 100 * f_bwd / (bwd_ms * 1e-3) / 1e12 / DATASHEET_BF16_TFLOPS,
+                "peak_tflops": DATASHEET_BF16_TFLOPS, "source": DATASHEET_SOURCE},
             "kernel_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
                           "bwd_dq_convert": conv_ms},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved,
@@ -477,6 +618,7 @@ def run_gpu(args, cfg, name):
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "kvcache_decode": kvc,
+            "workloads": table,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -863,6 +1005,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kvcache", action="store_true",
                     help="skip the KV-cache decode figure of the default line")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload table (all five workloads) of the default line")
     ap.add_argument("--e2e-chunk-heads", type=int, default=8,
                     help="heads per chunk of the end-to-end pipeline (largest divisor of H "
                          "not above this)")

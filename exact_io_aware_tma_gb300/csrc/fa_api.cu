@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "../../include/fa.h"
+#include "../../include/fa_selftest.h"
 #include "fa_common.cuh"
 #include "fa_kernels.h"
 
@@ -605,6 +606,52 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
   dq_convert_packed_kernel<<<elementwise_blocks(chunks), 256, 0, s>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), scale, H, total, d);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_selftest_forward_lost_signal(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int H, int N, int d, float scale,
+                                    int causal, void* stream) {
+  const fa_mask m = plain_mask(causal, nullptr, nullptr);
+  Problem p;
+  int st = check_sizes(B, H, N, d, scale, &m, &p);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  p.status = status_word();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  cudaError_t e = launch_fwd_tc_lost_signal(p, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_selftest_backward_lost_signal(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout, void* dq, void* dk,
+                                     void* dv, int B, int H, int N, int d, float scale,
+                                     int causal, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  const fa_mask m = plain_mask(causal, nullptr, nullptr);
+  Problem p;
+  int st = check_sizes(B, H, N, d, scale, &m, &p);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  st = check_workspace(B, H, N, d, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  p.status = status_word();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  st = fa_backward_preprocess(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  const long long heads = (long long)B * H;
+  cudaError_t e = launch_bwd_tc_lost_signal(
+      p, q, k, v, dout, ws_lse2(workspace), ws_dvec(workspace, heads, N),
+      ws_dq_acc(workspace, heads, N), dk, dv, padded_rows(N), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
 
 int fa_last_device_status(void* stream) {

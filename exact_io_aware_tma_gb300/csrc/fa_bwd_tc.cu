@@ -114,7 +114,11 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
   return false;
 }
 
-template <int D, bool PACKED, bool DROP, bool SPLIT>
+// LOSE: self-test instantiation only (fa_selftest_backward_lost_signal): the
+// first element-wise warp withholds its arrival for the first query step
+// and every wait gives up after 1 ms, so the gradient issuer's wait runs out
+// and the abort, drain and status paths run.
+template <int D, bool PACKED, bool DROP, bool SPLIT, bool LOSE = false>
 __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   auto bar = [&](int i) { return bar0 + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
-  const Abort ab{abort_flag, p.status};
+  const Abort ab{abort_flag, p.status, LOSE ? kShortWaitLimitNs : kWaitLimitNs};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int klim = key_limit(p, b);
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_EW + bf));
+      if (lane == 0 && !(LOSE && i == 0 && warp == 4)) mbar_arrive(bar(C::B_EW + bf));
     }
     // ---- epilogue: dK (x scale), dV -> bf16 -> shared (swizzled) -> TMA store;
     // in the packed layout a key tile that ends past its sequence is written
@@ -726,7 +730,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int D, bool PACKED, bool DROP, bool SPLIT>
+template <int D, bool PACKED, bool DROP, bool SPLIT, bool LOSE = false>
 static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void* k,
                                    const void* v, const void* dout, const float* lse2,
                                    const float* dvec, float* dq_acc, void* dk, void* dv, int npad,
@@ -758,18 +762,18 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
   if (!maps) return cudaErrorInvalidValue;
   cudaError_t e;
   if constexpr (SPLIT) {
-    static int nsm = 0;
-    if (nsm == 0) {
-      int dev = 0;
-      if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-      if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return e;
-    }
+    // the current device's SM count, asked on every call (a few hundred
+    // nanoseconds; a process-wide cache would be wrong across devices and
+    // racy across host threads)
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
     bwd_plan_kernel<<<1, 1024, 0, st>>>(p, nsm, bh, const_cast<int4*>(split.items),
                                         const_cast<int*>(split.nitems));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT>;
+  auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT, LOSE>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
@@ -795,6 +799,16 @@ static cudaError_t launch_bwd_tc_d(const Problem& p, const void* q, const void* 
                                                               dq_acc, dk, dv, npad, split, st)
                    : launch_bwd_tc_t<128, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
                                                                dq_acc, dk, dv, npad, split, st);
+}
+
+cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
+                                      const void* v, const void* dout, const float* lse2,
+                                      const float* dvec, float* dq_acc, void* dk, void* dv,
+                                      int npad, cudaStream_t st) {
+  if (p.d != 128 || p.cu_seqlens != nullptr || p.drop_p8 != 0) return cudaErrorInvalidValue;
+  const BwdSplit none{nullptr, nullptr, nullptr};
+  return launch_bwd_tc_t<128, false, false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc,
+                                                         dk, dv, npad, none, st);
 }
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,

@@ -102,7 +102,11 @@ __device__ __forceinline__ bool live_bit(const uint32_t* live, int i, int first,
   return (live[i * kFwdLiveWords + (t >> 5)] >> (t & 31)) & 1u;
 }
 
-template <int D, bool PACKED, bool DROP, bool SOLO>
+// LOSE: self-test instantiation only (fa_selftest_forward_lost_signal): the
+// first softmax warp withholds its P-ready arrival for the first key tile
+// and every wait gives up after 1 ms, so the MMA issuer's wait runs out and
+// the abort, drain and status paths run.
+template <int D, bool PACKED, bool DROP, bool SOLO, bool LOSE = false>
 __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
   auto bar = [&](int i) { return bar0 + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
-  const Abort ab{abort_flag, p.status};
+  const Abort ab{abort_flag, p.status, LOSE ? kShortWaitLimitNs : kWaitLimitNs};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = npairs - 1 - yi;  // heaviest causal pairs first
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_P + i));
+        if (lane == 0 && !(LOSE && n == 0 && warp == C::WARP_SM)) mbar_arrive(bar(C::B_P + i));
         ++n;
       }
       // ---- epilogue: O = u / l -> bf16 -> shared (swizzled) -> TMA store;
@@ -533,7 +537,7 @@ static int heads_per_group(long long heads, long long bytes_per_head) {
   return (int)g;
 }
 
-template <int D, bool PACKED, bool DROP, bool SOLO>
+template <int D, bool PACKED, bool DROP, bool SOLO, bool LOSE = false>
 static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void* k,
                                    const void* v, void* o, float* lse, cudaStream_t st) {
   using C = FwdTc<D, SOLO>;
@@ -551,7 +555,7 @@ static cudaError_t launch_fwd_tc_t(const Problem& pin, const void* q, const void
     maps = make_bf16_map_3d(&tq, q, D, p.N, bh, 128) && make_bf16_map_3d(&tk, k, D, p.N, bh, 128) &&
            make_bf16_map_3d(&tv, v, D, p.N, bh, 128) && make_bf16_map_3d(&to, o, D, p.N, bh, 128);
   if (!maps) return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D, PACKED, DROP, SOLO>;
+  auto kern = fwd_tc_kernel<D, PACKED, DROP, SOLO, LOSE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -596,6 +600,12 @@ static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* 
   if constexpr (!PACKED && !DROP)
     if (use_solo(p)) return launch_fwd_tc_t<128, false, false, true>(p, q, k, v, o, lse, st);
   return launch_fwd_tc_t<128, PACKED, DROP, false>(p, q, k, v, o, lse, st);
+}
+
+cudaError_t launch_fwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
+                                      const void* v, void* o, float* lse, cudaStream_t st) {
+  if (p.d != 128 || p.cu_seqlens != nullptr || p.drop_p8 != 0) return cudaErrorInvalidValue;
+  return launch_fwd_tc_t<128, false, false, false, true>(p, q, k, v, o, lse, st);
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* o,

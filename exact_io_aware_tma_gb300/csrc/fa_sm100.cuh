@@ -13,6 +13,9 @@ namespace sm100 {
 // A wait that has not completed after this long (ns) is treated as lost: the
 // waiter records FA_ERR_TIMEOUT and the CTA winds down instead of hanging.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// The limit of the self-test instantiations that withhold one arrival on
+// purpose (so that a wait runs out quickly).
+constexpr uint64_t kShortWaitLimitNs = 1000000ull;
 constexpr int kStatusTimeout = 4;  // FA_ERR_TIMEOUT
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -58,24 +61,12 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Tests two barriers with both probes in flight together.
-__device__ __forceinline__ bool mbar_test2(uint32_t bar0, uint32_t par0, uint32_t bar1,
-                                           uint32_t par1) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p, q;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n"
-      " and.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar0), "r"(par0), "r"(bar1), "r"(par1)
-      : "memory");
-  return ok != 0;
-}
 
 // Shared abort word of a CTA plus the global status word.
 struct Abort {
-  volatile int* flag;  // shared memory
-  int* status;         // global
+  volatile int* flag;                 // shared memory
+  int* status;                        // global
+  uint64_t limit_ns = kWaitLimitNs;   // how long a wait may take
 };
 
 // Waits until the phase of `bar` with parity `parity` has completed.  Returns
@@ -87,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > ab.limit_ns) {
       *ab.flag = 1;
       atomicExch(ab.status, kStatusTimeout);
       return false;
@@ -113,16 +104,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// Reduce-add a shared-memory fp32 tile into global memory (element-wise
-// atomic add performed by the TMA unit); rows outside the map are skipped.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0,
-                                                  int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 // Plain (untensored) bulk copy global -> shared; both addresses 16-byte
 // aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -138,9 +119,6 @@ __device__ __forceinline__ void tma_store_commit() {
 }
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Makes generic-proxy shared-memory writes visible to the async proxy (TMA
 // store, tcgen05.mma operand reads).
@@ -518,27 +496,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
-// TMEM -> registers: two blocks of 32 lanes x 32 columns, one wait.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(a0), "r"(a1)
-      : "memory");
-}
 
-// Read-only 16-byte global load kept at its place in the instruction stream
-// (so the compiler does not hoist a batch of them and raise register
-// pressure).
-__device__ __forceinline__ float4 ldg_f4_inplace(const float4* ptr) {
-  float4 v;
-  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(ptr));
-  return v;
-}
 
 // ---- packed fp32 arithmetic (two lanes per instruction) and 3-input max
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
@@ -584,9 +542,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t elect_one_lane() {
-  return (threadIdx.x & 31) == 0;
-}
 
 }  // namespace sm100
 }  // namespace fa

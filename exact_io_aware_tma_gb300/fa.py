@@ -32,6 +32,8 @@ SIGNATURES = {
     "fa_tile_schedule": ([_i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
     "fa_last_device_status": ([_vp], _i),
     "fa_selftest_mma": ([_i, _vp, _vp, _vp, _i, _vp], _i),
+    "fa_selftest_forward_lost_signal": ([_vp] * 5 + [_i] * 4 + [_f, _i, _vp], _i),
+    "fa_selftest_backward_lost_signal": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _sz, _vp], _i),
     "fa_backward_noalloc": ([_vp] * 9 + [_i] * 4 + [_f, _i, _vp, _vp, _vp], _i),
     "fa_forward_masked": ([_vp] * 5 + [_i] * 4 + [_f, _vp, _vp], _i),
     "fa_backward_masked": ([_vp] * 9 + [_i] * 4 + [_f, _vp, _vp, _sz, _vp], _i),

@@ -231,8 +231,16 @@ FA_API int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float sc
  * library and held until the process exits.  Nothing is allocated.
  *  - Problems whose fa_backward_workspace_bytes() exceeds
  *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_INVALID_ARG before
- *    any CUDA call (32 MiB covers e.g. B*H*N*d up to about 8 million
- *    elements).
+ *    any CUDA call.  That size is 2 * r(4*B*H*Np) + r(4*B*H*N*d) bytes,
+ *    with Np = N rounded up to a multiple of 128 and r() rounding up to a
+ *    multiple of 256; call fa_backward_workspace_bytes() to test a shape
+ *    (e.g. B*H = 16, N = 8192, d = 64 needs 33.0 MiB and is rejected; at
+ *    N = 7680 it needs 30.9 MiB and fits).
+ *  - With a block mask the spare room of the array beyond that size, when
+ *    there is enough of it, lets the backward split heavy key tiles over
+ *    several CTAs exactly as fa_backward does given
+ *    fa_backward_workspace_bytes_masked() bytes; otherwise it runs unsplit.
+ *    The results agree either way.
  *  - The first call on a device looks up the array's device address on that
  *    device (the current device) and caches it; make that first call before
  *    any stream capture.

@@ -44,6 +44,31 @@ extern "C" {
 FA_API int fa_selftest_mma(int mode, const void* a, const void* b, float* c, int n,
                            void* stream);
 
+/*
+ * Self-test of the bounded waits (failure detection without a GPU fault).
+ * Every mbarrier wait in the attention kernels gives up after a time limit,
+ * records FA_ERR_TIMEOUT in the library's device error word, makes the other
+ * warps of its CTA stop, lets the CTA's copies and tensor-core work in
+ * flight finish (again with bounded waits), frees its tensor memory and
+ * exits, so a lost signal cannot hang the GPU.  These two entry points run
+ * that path on purpose: the same arguments as fa_forward / fa_backward
+ * (d = 128 only, no block mask or key lengths; FA_ERR_UNSUPPORTED for other
+ * d), but one warp of each CTA withholds one arrival (the forward's first
+ * softmax warp its P-ready signal for its first key tile; the backward's
+ * first element-wise warp its signal for the first query step) and the
+ * waits give up after 1 ms instead of 2 s.  The call returns FA_OK at
+ * launch; fa_last_device_status() then returns FA_ERR_TIMEOUT (and clears
+ * it), the outputs are unspecified, and the device stays usable.
+ */
+FA_API int fa_selftest_forward_lost_signal(const void* q, const void* k, const void* v, void* o,
+                                           float* lse, int B, int H, int N, int d, float scale,
+                                           int causal, void* stream);
+FA_API int fa_selftest_backward_lost_signal(const void* q, const void* k, const void* v,
+                                            const void* o, const float* lse, const void* dout,
+                                            void* dq, void* dk, void* dv, int B, int H, int N,
+                                            int d, float scale, int causal, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -51,3 +51,38 @@ def test_flops_of_the_five_workloads():
         cfg = WORKLOADS[name]
         fwd, _ = bench.flops(cfg, bench.dense_fraction(cfg))
         assert fwd == pytest.approx(w, rel=5e-3), name
+
+
+def test_key_padding_effective_fraction():
+    # BERT-shaped key padding: the effective pair fraction is the mean of
+    # kv_len[b] / N, every drawn length within [256, 512]
+    from exact_io_aware_tma_gb300.workloads import make_inputs
+    cfg = WORKLOADS["bert_large_keypad_n512_d64"]
+    inp = make_inputs(**cfg, with_grad=False)
+    lens = [int(x) for x in inp["kv_len"]]
+    assert all(256 <= x <= 512 for x in lens)
+    want = sum(lens) / (len(lens) * cfg["N"])
+    assert bench.effective_fraction(cfg, inp) == pytest.approx(want, rel=1e-15)
+    assert 0.5 <= bench.effective_fraction(cfg, inp) <= 1.0
+    # other masks report no effective figure
+    for name in ("gpt2_causal_n1024_d64", "tiny_dense_n128_d64"):
+        other = make_inputs(**WORKLOADS[name], with_grad=False)
+        assert bench.effective_fraction(WORKLOADS[name], other) is None
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_both_arms_name_the_same_config(name):
+    # the GPU arm and the oracle arm build `config` with one helper
+    cfg = WORKLOADS[name]
+    a = bench.workload_config(name, cfg, 1)
+    assert a == bench.workload_config(name, dict(cfg), 1)
+    assert a["workload"] == name and a["parallelism"] == "replicas1"
+    assert {"B", "H", "N", "d", "mask", "l2"} <= set(a)
+
+
+def test_datasheet_peak_matches_the_per_sm_rate():
+    # 2.5 PFLOP/s dense (half the sparse per-GPU figure) is within 4% of
+    # 152 SMs x 8192 dense bf16 FLOP per clock x the 2.07 GHz maximum clock
+    derived = 152 * 8192 * 2.07e9 / 1e12
+    assert bench.DATASHEET_BF16_TFLOPS == 2500.0
+    assert abs(derived - bench.DATASHEET_BF16_TFLOPS) / derived < 0.04

@@ -42,3 +42,37 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st = lib.fa_backward_noalloc(p, p, p, p, fa._ptr(lse), p, p, p, p, 64, 16, 8192, 128,
                                  0.1, 0, None, None, fa._stream())
     assert st == fa.FA_ERR_INVALID_ARG
+
+
+def test_noalloc_block_mask_against_the_oracle():
+    # A block mask with global key columns: the array's room beyond the base
+    # workspace lets the backward split those heavy key tiles (plan items and
+    # fp32 part slots in the shared array).  Two calls in a row with
+    # different masks and inputs, each against the fp64 oracle and against
+    # fa_backward given the masked (split) workspace.
+    from exact_io_aware_tma_gb300.workloads import band_global_block_mask, to_f64
+    from oracle import attention_backward
+    B, H, N, d = 1, 2, 1024, 64
+    T = N // 128
+    for call, (seed, band, every) in enumerate(((23, 1, 4), (24, 0, 3))):
+        bm_np = band_global_block_mask(T, band, every)
+        inp = make_inputs(B=B, H=H, N=N, d=d, mask="none", seed=seed)
+        g = to_device(inp)
+        bm = torch.from_numpy(bm_np).cuda()
+        assert fa.backward_workspace_bytes(B, H, N, d, bm) <= fa.NOALLOC_SCRATCH_BYTES
+        o, lse = fa.forward(g["q"], g["k"], g["v"], block_mask=bm, scale=g["scale"])
+        got = fa.backward_noalloc(g["q"], g["k"], g["v"], o, lse, g["do"], block_mask=bm,
+                                  scale=g["scale"])
+        ws = torch.empty(fa.backward_workspace_bytes(B, H, N, d, bm), device="cuda",
+                         dtype=torch.uint8)
+        want = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], block_mask=bm,
+                           scale=g["scale"], workspace=ws)
+        torch.cuda.synchronize()
+        assert fa.last_device_status() == fa.FA_OK
+        q, k, v, do = (to_f64(inp[x]) for x in ("q", "k", "v", "do"))
+        ref = attention_backward(q, k, v, do, inp["scale"], False, bm_np, None)
+        for name, a, b, r in zip(("dQ", "dK", "dV"), got, want, ref[:3]):
+            a = a.double().cpu().numpy()
+            check_close(f"{name} vs oracle (call {call})", a, r, TOL_GRAD)
+            check_close(f"{name} vs fa_backward (call {call})", a, b.double().cpu().numpy(),
+                        TOL_GRAD)
