@@ -31,10 +31,14 @@
 //               the warp), so the dQ tile costs no shared-memory traffic.
 //
 // TMEM columns: dV [0,d), dK [d,2d), S[b] = 2d + 64b, dP[b] = 2d + 128 + 64b
-// for the two step buffers b; dQ^T of step i is written over dP[i % 2] once
-// the element-wise warps have consumed dP^T(i), and dP^T(i+2) waits until
-// the dQ warps have read dQ^T(i) out.  For d = 64 the dQ^T product is issued
-// with M = 128 (the second 64 rows read the V tile and are discarded).
+// for the two step buffers b.  At d = 64 dQ^T has two buffers of its own,
+// dQ[b] = 384 + 64b, so the recompute GEMMs never wait for the dQ warps.
+// At d = 128 the 512 columns are full: dQ^T of step i is written over
+// dP[i % 2] once the element-wise warps have consumed dP^T(i) (it is the
+// first gradient GEMM of the step, so that the dQ warps read it out early),
+// and dP^T(i+2) waits until they have.  For d = 64 the dQ^T product is
+// issued with M = 128 (the second 64 rows read the V tile and are
+// discarded).
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -49,6 +53,12 @@ template <int D>
 struct BwdTc {
   static constexpr int THREADS = 384;
   static constexpr int BQ = 64;                 // query rows per step
+  // dQ^T in TMEM buffers of its own and reduced through shared memory by
+  // TMA reduce-adds (d = 64), or over dP^T and reduced by the dQ warps with
+  // atomics from registers (d = 128, where TMEM and shared memory are full)
+  static constexpr bool SEPQ = D == 64;
+  // dQ warps holding TMEM lanes below d (the others have nothing to do)
+  static constexpr int DQ_WARPS = D / 32;
   static constexpr int NS = D == 128 ? 3 : 4;   // step stages
   static constexpr int HALF_K = 128 * 128;      // [128 rows][64 cols] bf16 box
   static constexpr int HALF_Q = 64 * 128;       // [64 rows][64 cols] bf16 box
@@ -60,9 +70,10 @@ struct BwdTc {
   static constexpr int OFF_DS = (OFF_VEC + NS * 512 + 1023) / 1024 * 1024;
   static constexpr int DS = 128 * BQ * 2;             // dS^T [128 keys][64 q] bf16, x2
   static constexpr int OFF_BAR = OFF_DS + 2 * DS;
+  // B_DSF[b]: the gradient GEMMs that read dS^T buffer b have completed
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_S = 1 + 2 * NS, B_EW = B_S + 2,
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
-                       B_DRAIN = B_FIN + 1, NBAR = B_DRAIN + 2;
+                       B_DRAIN = B_FIN + 1, B_DSF = B_DRAIN + 2, NBAR = B_DSF + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // misc: TMEM address (+0), abort flag (+16) and the split item's part
   // word (+44)
@@ -72,8 +83,15 @@ struct BwdTc {
   // live query tiles of the key tile's range under a block mask, one bit each
   static constexpr int OFF_LIVE = OFF_DROP + 2 * DROPB;
   static constexpr int LIVEB = 65536 / 8;
-  static constexpr int SMEM = OFF_LIVE + LIVEB + 1024;
+  // d = 64: the step's dQ rows, [64 rows][32 columns] fp32 per dQ warp (two
+  // warps), two buffers, added into the accumulator by TMA reduce-adds
+  static constexpr int DQW = BQ * 32 * 4;
+  static constexpr int DQS = 2 * DQW;
+  static constexpr int OFF_DQS = (OFF_LIVE + LIVEB + 1023) / 1024 * 1024;
+  static constexpr int SMEM = (SEPQ ? OFF_DQS + 2 * DQS : OFF_LIVE + LIVEB) + 1024;
   static constexpr int COL_DV = 0, COL_DK = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
+  static constexpr int COL_DQ = SEPQ ? 2 * D + 256 : COL_DP;
+  static_assert(!SEPQ || COL_DQ + 128 <= 512, "TMEM columns");
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(2 * KT <= NS * STAGE, "dK/dV staging must fit in the stage ring");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -123,7 +141,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                  const Problem pin, const float* __restrict__ lse2, const float* __restrict__ dvec,
+                  const __grid_constant__ CUtensorMap tm_dq, const Problem pin, const float* __restrict__ lse2, const float* __restrict__ dvec,
                   float* __restrict__ dq_acc, int npad, __nv_bfloat16* __restrict__ dk_rows,
                   __nv_bfloat16* __restrict__ dv_rows, const BwdSplit sp) {
   using C = BwdTc<D>;
@@ -176,8 +194,9 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
-      const bool four = (i == C::B_EW || i == C::B_EW + 1 || i == C::B_DQE || i == C::B_DQE + 1);
-      mbar_init(bar(i), four ? 4 : 1);
+      const bool ew = i == C::B_EW || i == C::B_EW + 1;
+      const bool dqe = i == C::B_DQE || i == C::B_DQE + 1;
+      mbar_init(bar(i), ew ? 4 : dqe ? C::DQ_WARPS : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -230,7 +249,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       int qt = -1, sub = 0, slot = 0, round = 0;
       while (next_q_step<D>(p, kt, klim, smem, qt, sub)) {
         const int q0 = qt * 128 + sub * 64;
-        if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) break;
+        if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab, kSleepHintNs)) break;
         const uint32_t st = s0 + C::OFF_ST + slot * C::STAGE;
         const uint32_t fb = bar(C::B_FULL + slot);
         const uint32_t vb = s0 + C::OFF_VEC + slot * 512;
@@ -266,9 +285,11 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     // long as a narrow MMA takes to run, so one thread cannot feed the tensor
     // core with all five GEMMs of a step and its barrier polls.
     //   warp 1: S^T(j), dP^T(j) into buffer j % 2 (owns TMEM);
-    //   warp 2: dV(i), dK(i), dQ^T(i) over dP[i % 2].
+    //   warp 2: d = 64: dV(i), dK(i), dQ^T(i) into dQ[i % 2];
+    //           d = 128: dQ^T(i) over dP[i % 2], dV(i), dK(i).
     // S^T(j) waits until dV(j-2) has read P^T(j-2) from the same columns
-    // (s_free), dP^T(j) until the dQ warps have read dQ^T(j-2) out.
+    // (s_free); at d = 128 dP^T(j) waits until the dQ warps have read
+    // dQ^T(j-2) out, at d = 64 dQ^T(i) waits for that instead.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, C::BQ, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
@@ -298,7 +319,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
             mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
           else
             mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
-          if (j >= 2) {
+          if (!C::SEPQ && j >= 2) {
             if (!(ok = mbar_wait(bar(C::B_DQE + bf), ((j - 2) >> 1) & 1, ab))) break;
             tc_fence_after();
           }
@@ -315,15 +336,28 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
           const uint64_t ds = dds + (uint64_t)(bf * ds_step);
           if (!(ok = mbar_wait(bar(C::B_EW + bf), (i >> 1) & 1, ab))) break;
           tc_fence_after();
+          if constexpr (!C::SEPQ) {
+            // dQ^T = K^T dS^T over dP[bf] (dP^T(i) is in the element-wise
+            // warps' registers by now)
+            mma_ss_mn_mn_k128(tmem + C::COL_DQ + 64 * bf, dk_mn, ds, id_q, 0);
+            mma_commit(bar(C::B_DQF + bf));
+          }
           // dV += P^T dO   (P^T: bf16 in TMEM over S[bf]; dO as MN-major B)
           mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
           mma_commit(bar(C::B_SF + bf));
           // dK += dS^T Q
           mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, i > 0);
           mma_commit(bar(C::B_EMPTY + i % C::NS));
-          // dQ^T = K^T dS^T over dP[bf]
-          mma_ss_mn_mn_k128(tmem + C::COL_DP + 64 * bf, dk_mn, ds, id_q, 0);
-          mma_commit(bar(C::B_DQF + bf));
+          if constexpr (C::SEPQ) {
+            // dQ^T = K^T dS^T into dQ[bf], once dQ^T(i-2) has been read out
+            if (i >= 2) {
+              if (!(ok = mbar_wait(bar(C::B_DQE + bf), ((i - 2) >> 1) & 1, ab))) break;
+              tc_fence_after();
+            }
+            mma_ss_mn_mn_k128(tmem + C::COL_DQ + 64 * bf, dk_mn, ds, id_q, 0);
+            mma_commit(bar(C::B_DQF + bf));
+          }
+          mma_commit(bar(C::B_DSF + bf));
         }
         // dK and dV are complete once this thread's last MMAs are (the other
         // issuer's work for the last step finished before it could start)
@@ -443,7 +477,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of
       // step i-2 (which read this buffer) have completed.
       if (i >= 2) {
-        if (!(ok = mbar_wait(bar(C::B_DQF + bf), ((i - 2) >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait(bar(C::B_DSF + bf), ((i - 2) >> 1) & 1, ab))) break;
       }
       uint8_t* dsb = smem + C::OFF_DS + bf * C::DS + r * 128;
 #pragma unroll
@@ -540,35 +574,64 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ
     const int c = ((warp & 3) << 5) + lane;  // head-dim index = TMEM lane
-    const bool valid = c < D;
+    const bool valid = c < D;                 // the same for the whole warp
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int qt = -1, sub = 0;
     bool ok = true;
-    for (int i = 0; next_q_step<D>(p, kt, klim, smem, qt, sub); ++i) {
+    for (int i = 0; valid && next_q_step<D>(p, kt, klim, smem, qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
-      if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab))) break;
+      if (!(ok = mbar_wait(bar(C::B_DQF + bf), (i >> 1) & 1, ab, kSleepHintNs))) break;
       tc_fence_after();
       uint32_t v[64];
-      if (valid) tmem_ld64(lane_base + C::COL_DP + 64 * bf, v);
+      if (valid) tmem_ld64(lane_base + C::COL_DQ + 64 * bf, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_DQE + bf));
-      // Reduce into the fp32 accumulator straight from registers: for each
-      // query the warp's 32 lanes add 32 consecutive floats of its row.
-      if (valid) {
-        const int rows = min(64, p.N - q0);
-        // padded: [B*H][N][d]; packed: [H][total][d] (head-major, so a head's
-        // rows are contiguous and the reductions do not collide in L2 the way
-        // rows H*d apart do)
-        const size_t row_stride = (size_t)D;
-        float* dst = PACKED ? dq_acc + ((size_t)head * p.total + start + q0) * D + c
-                            : dq_acc + ((size_t)bh * p.N + q0) * D + c;
+      // padded: [B*H][N][d]; packed: [H][total][d] (head-major, so a head's
+      // rows are contiguous and the reductions do not collide in L2 the way
+      // rows H*d apart do)
+      const int rows = min(64, p.N - q0);
+      float* dst_rows = PACKED ? dq_acc + ((size_t)head * p.total + start + q0) * D
+                               : dq_acc + ((size_t)bh * p.N + q0) * D;
+      if constexpr (C::SEPQ) {
+        // d = 64: each dQ warp writes its 32 columns of the step's rows to
+        // its own shared buffer (a warp instruction stores 32 consecutive
+        // floats of one row: conflict-free) and its lane 0 adds the tile
+        // into the accumulator with a TMA reduce-add (rows outside the
+        // tensor are skipped; in the packed layout the rows past this
+        // sequence carry exact zeros, since their dS is masked to 0).  The
+        // buffer of step i is rewritten at step i + 2, once that reduce has
+        // read it.
+        if (valid) {
+          float* stg = reinterpret_cast<float*>(smem + C::OFF_DQS + (i & 1) * C::DQS +
+                                                (warp & 3) * C::DQW);
+          if (lane == 0 && i >= 2) bulk_wait_read_1();
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 64; ++q) stg[q * 32 + lane] = __uint_as_float(v[q]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (PACKED)
+              tma_reduce_add_3d(&tm_dq, smem_u32(stg), 32 * (warp & 3), start + q0, head);
+            else
+              tma_reduce_add_3d(&tm_dq, smem_u32(stg), 32 * (warp & 3), q0, (int)bh);
+            tma_store_commit();
+          }
+        }
+      } else {
+        // d = 128: straight from registers: for each query the warp's 32
+        // lanes add 32 consecutive floats of its row.  (Vector reductions
+        // after a 4 x 4 shuffle transpose measured 16% slower here.)
+        float* dst = dst_rows + c;
 #pragma unroll
         for (int q = 0; q < 64; ++q)
-          if (q < rows) atomicAdd(dst + (size_t)q * row_stride, __uint_as_float(v[q]));
+          if (q < rows) atomicAdd(dst + (size_t)q * D, __uint_as_float(v[q]));
       }
     }
+    // the reduce-adds of the last steps have read their shared memory
+    if (C::SEPQ && valid && lane == 0) tma_store_wait_read();
   }
   tc_fence_before();
   __syncthreads();
@@ -745,7 +808,7 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
     p.hgroup = (int)(g < 1 ? 1 : (g > heads ? heads : g));
   }
   const long long bh = (long long)p.B * p.H;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
   bool maps;
   if constexpr (PACKED)
     maps = make_bf16_map_packed(&tq, q, D, p.H, p.total, C::BQ) &&
@@ -753,12 +816,14 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
            make_bf16_map_packed(&tv, v, D, p.H, p.total, 128) &&
            make_bf16_map_packed(&tdo, dout, D, p.H, p.total, C::BQ) &&
            make_bf16_map_packed(&tdk, dk, D, p.H, p.total, 128) &&
-           make_bf16_map_packed(&tdv, dv, D, p.H, p.total, 128);
+           make_bf16_map_packed(&tdv, dv, D, p.H, p.total, 128) &&
+           make_f32_map_3d(&tdq, dq_acc, D, p.total, p.H, C::BQ, 32);
   else
     maps = make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) &&
            make_bf16_map_3d(&tk, k, D, p.N, bh, 128) && make_bf16_map_3d(&tv, v, D, p.N, bh, 128) &&
            make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) &&
-           make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) && make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128);
+           make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) && make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128) &&
+           make_f32_map_3d(&tdq, dq_acc, D, p.N, bh, C::BQ, 32);
   if (!maps) return cudaErrorInvalidValue;
   cudaError_t e;
   if constexpr (SPLIT) {
@@ -777,7 +842,8 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, p, lse2, dvec, dq_acc, npad,
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, lse2, dvec, dq_acc,
+                                          npad,
                                           static_cast<__nv_bfloat16*>(dk),
                                           static_cast<__nv_bfloat16*>(dv), split);
   if constexpr (SPLIT) {

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
       for (int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1); kt < p.T && ok;
            kt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt)) {
         for (int which = 0; which < 2; ++which) {
-          if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab)) {
+          if (!mbar_wait(bar(C::B_EMPTY + slot), (round & 1) ^ 1, ab, kSleepHintNs)) {
             ok = false;
             break;
           }

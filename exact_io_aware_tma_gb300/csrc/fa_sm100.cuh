@@ -50,6 +50,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but the thread may stay suspended until the phase completes
+// or up to `hint_ns` nanoseconds have passed (instead of the hardware's own,
+// short, limit), so a waiting thread does not keep re-issuing the test and
+// take issue slots from the other warps of its SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking test of the same condition (no suspend window).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -69,14 +85,26 @@ struct Abort {
   uint64_t limit_ns = kWaitLimitNs;   // how long a wait may take
 };
 
+// Suspension hints (ns) of the two kinds of waits.  Latency-critical waiters
+// (MMA issuers, softmax / element-wise warps) poll (hint 0: the hardware's
+// own short suspension), since a thread sleeping in the barrier resumes up
+// to about a microsecond after the phase completes.  Background waiters (the
+// TMA producer, the dQ warps) sleep in the barrier, so that they do not take
+// issue slots from the critical warps of their SM sub-partition; the abort
+// flag and the time limit are re-checked at least this often.
+constexpr uint32_t kPollHintNs = 0;
+constexpr uint32_t kSleepHintNs = 20000;
+
 // Waits until the phase of `bar` with parity `parity` has completed.  Returns
 // false (and raises the CTA's abort flag and the global status) on timeout,
 // or false at once if another warp of the CTA already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab,
+                                          uint32_t hint_ns = kPollHintNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (hint_ns != 0 ? mbar_try_wait_sleep(bar, parity, hint_ns) : mbar_try_wait(bar, parity))
+      return true;
     if (*ab.flag) return false;
     if (globaltimer() - t0 > ab.limit_ns) {
       *ab.flag = 1;
@@ -113,6 +141,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+// Element-wise add of a shared-memory tile into the global tensor of `map`
+// (a reduce-add performed by the TMA unit); elements outside the tensor are
+// skipped.  The innermost coordinate times the element size must be a
+// multiple of 16 bytes, and no coordinate may be negative.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// Waits until at most one committed bulk group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");

@@ -94,15 +94,16 @@ inline bool make_bf16_map_sw32(CUtensorMap* m, const void* base, int row_elems, 
   return r == CUDA_SUCCESS;
 }
 
-// fp32 tensor viewed as [heads][rows][cols], boxes of cols x box_rows, no
-// swizzle (plain row-major tile in shared memory); used for reduce-adds.
+// fp32 tensor viewed as [heads][rows][cols], boxes of box_cols (all cols if
+// 0) x box_rows, no swizzle (plain row-major tile in shared memory); used
+// for reduce-adds.
 inline bool make_f32_map_3d(CUtensorMap* m, const void* base, int cols, int rows,
-                            long long heads, int box_rows) {
+                            long long heads, int box_rows, int box_cols = 0) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * 4 * (cuuint64_t)rows};
-  cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(box_cols > 0 ? box_cols : cols), (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
