@@ -49,9 +49,18 @@
 namespace fa {
 using namespace sm100;
 
+// Element-wise warpgroups: at d = 64 (no dropout) two groups of four warps
+// share each step, one per 32 queries, since there the element-wise work of
+// a step outlasts its MMAs; otherwise one group of four takes all 64.
+template <int D, bool DROP>
+struct BwdEw {
+  static constexpr int GROUPS = (D == 64 && !DROP) ? 2 : 1;
+  static constexpr int QH = 64 / GROUPS;           // queries per thread and step
+  static constexpr int THREADS = 256 + 128 * GROUPS;
+};
+
 template <int D>
 struct BwdTc {
-  static constexpr int THREADS = 384;
   static constexpr int BQ = 64;                 // query rows per step
   // dQ^T in TMEM buffers of its own and reduced through shared memory by
   // TMA reduce-adds (d = 64), or over dP^T and reduced by the dQ warps with
@@ -137,7 +146,7 @@ __device__ __forceinline__ bool next_q_step(const Problem& p, int kt, int klim,
 // and every wait gives up after 1 ms, so the gradient issuer's wait runs out
 // and the abort, drain and status paths run.
 template <int D, bool PACKED, bool DROP, bool SPLIT, bool LOSE = false>
-__global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
+__global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -145,6 +154,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
                   float* __restrict__ dq_acc, int npad, __nv_bfloat16* __restrict__ dk_rows,
                   __nv_bfloat16* __restrict__ dv_rows, const BwdSplit sp) {
   using C = BwdTc<D>;
+  using EW = BwdEw<D, DROP>;
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
   // (coordinates (x, h, start + row)), whose length then plays the role of N.
@@ -196,7 +206,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       const bool ew = i == C::B_EW || i == C::B_EW + 1;
       const bool dqe = i == C::B_DQE || i == C::B_DQE + 1;
-      mbar_init(bar(i), ew ? 4 : dqe ? C::DQ_WARPS : 1);
+      mbar_init(bar(i), ew ? 4 * EW::GROUPS : dqe ? C::DQ_WARPS : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       if (threadIdx.x == 0) reinterpret_cast<int*>(smem + C::OFF_MISC)[11] = item.w;
     }
     const int n = ql - qf + 1;
-    for (int wi = warp; wi < ((n + 31) >> 5); wi += C::THREADS / 32) {
+    for (int wi = warp; wi < ((n + 31) >> 5); wi += EW::THREADS / 32) {
       const int t = (wi << 5) + lane;
       const bool in_part = !SPLIT || (qf + t >= item.y && qf + t <= item.z);
       const uint32_t bits =
@@ -342,8 +352,12 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
             mma_ss_mn_mn_k128(tmem + C::COL_DQ + 64 * bf, dk_mn, ds, id_q, 0);
             mma_commit(bar(C::B_DQF + bf));
           }
-          // dV += P^T dO   (P^T: bf16 in TMEM over S[bf]; dO as MN-major B)
-          mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
+          // dV += P^T dO   (P^T: bf16 in TMEM over S[bf], in two halves 32
+          // columns apart with two element-wise groups; dO as MN-major B)
+          if constexpr (EW::GROUPS == 2)
+            mma_ts_mn_k64_gap32(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
+          else
+            mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
           mma_commit(bar(C::B_SF + bf));
           // dK += dS^T Q
           mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, i > 0);
@@ -368,8 +382,13 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       while (!mbar_try_wait(bar(C::B_DRAIN + warp - 1), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // ------------------------------------------------------------ element-wise
+    // group g (warps 4-7, or 12-15 with two groups) takes the step's queries
+    // qo .. qo + QH - 1
+    constexpr int QH = EW::QH;
+    const int g = warp >= 12 ? 1 : 0;
+    const int qo = g * QH;
     const int r = ((warp & 3) << 5) + lane;  // key row within the tile
     const int j = kt * 128 + r;              // key index
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -380,8 +399,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
       const uint8_t* vb = smem + C::OFF_VEC + (i % C::NS) * 512;
-      const float* l2 = reinterpret_cast<const float*>(vb);
-      const float* dv = reinterpret_cast<const float*>(vb + 256);
+      const float* l2 = reinterpret_cast<const float*>(vb) + qo;
+      const float* dv = reinterpret_cast<const float*>(vb + 256) + qo;
       // Dropout: the step's 64 x 128 keep bytes, generated by the four warps
       // together (four generator calls per thread, each 16 keys of one
       // query) while the tensor core computes S^T and dP^T, stored with the
@@ -401,9 +420,14 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       }
       if (!(ok = mbar_wait(bar(C::B_S + bf), (i >> 1) & 1, ab))) break;
       tc_fence_after();
-      uint32_t sr[64], pr[64];
-      tmem_ld64(lane_base + C::COL_S + 64 * bf, sr);
-      tmem_ld64(lane_base + C::COL_DP + 64 * bf, pr);
+      uint32_t sr[QH], pr[QH];
+      if constexpr (QH == 64) {
+        tmem_ld64(lane_base + C::COL_S + 64 * bf, sr);
+        tmem_ld64(lane_base + C::COL_DP + 64 * bf, pr);
+      } else {
+        tmem_ld32(lane_base + C::COL_S + 64 * bf + qo, sr);
+        tmem_ld32(lane_base + C::COL_DP + 64 * bf + qo, pr);
+      }
       // queries c of the step allowed for this key: lo <= c < hi.  Only
       // whether the step has disallowed queries is kept through the loop;
       // they are zeroed in the packed words afterwards.
@@ -419,11 +443,11 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       {
         int lo, hi;
         q_range(lo, hi);
-        edge = lo > 0 || hi < 64;
+        edge = lo > qo || hi < qo + QH;
       }
-      uint32_t pk[32], dk[32];
+      uint32_t pk[QH / 2], dk[QH / 2];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
+      for (int c4 = 0; c4 < QH / 4; ++c4) {
         const float4 L = reinterpret_cast<const float4*>(l2)[c4];
         const float4 Dd = reinterpret_cast<const float4*>(dv)[c4];
         float x0, x1, x2, x3;
@@ -465,15 +489,23 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
         // above, possibly non-finite, are discarded half-word by half-word)
         int lo, hi;
         q_range(lo, hi);
+        lo -= qo;
+        hi -= qo;
 #pragma unroll
-        for (int w = 0; w < 32; ++w) {
+        for (int w = 0; w < QH / 2; ++w) {
           const uint32_t keep = ((2 * w >= lo && 2 * w < hi) ? 0x0000ffffu : 0u) |
                                 ((2 * w + 1 >= lo && 2 * w + 1 < hi) ? 0xffff0000u : 0u);
           pk[w] &= keep;
           dk[w] &= keep;
         }
       }
-      tmem_st32(lane_base + C::COL_S + 64 * bf, pk);
+      // P^T (bf16 pairs) over the group's own S^T columns: columns 0-31
+      // with one group; 0-15 and 32-47 with two (each group overwrites only
+      // columns it has already read)
+      if constexpr (QH == 64)
+        tmem_st32(lane_base + C::COL_S + 64 * bf, pk);
+      else
+        tmem_st16(lane_base + C::COL_S + 64 * bf + qo, pk);
       // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of
       // step i-2 (which read this buffer) have completed.
       if (i >= 2) {
@@ -481,8 +513,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       }
       uint8_t* dsb = smem + C::OFF_DS + bf * C::DS + r * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        *reinterpret_cast<uint4*>(dsb + ((c8 ^ (r & 7)) << 4)) =
+      for (int c8 = 0; c8 < QH / 8; ++c8)
+        *reinterpret_cast<uint4*>(dsb + (((c8 + qo / 8) ^ (r & 7)) << 4)) =
             make_uint4(dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
       fence_proxy_async_smem();
       tmem_st_wait();
@@ -490,10 +522,11 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0 && !(LOSE && i == 0 && warp == 4)) mbar_arrive(bar(C::B_EW + bf));
     }
-    // ---- epilogue: dK (x scale), dV -> bf16 -> shared (swizzled) -> TMA store;
+    // ---- epilogue (group 0): dK (x scale), dV -> bf16 -> shared (swizzled) -> TMA store;
     // in the packed layout a key tile that ends past its sequence is written
     // row by row instead (a whole-tile store would overwrite the next
     // sequence's first rows).
+    if (g == 0) {
     if (ok) ok = mbar_wait(bar(C::B_FIN), 0, ab);
     tc_fence_after();
     // A part of a split key tile stores its fp32 dK, dV rows (0 if it ran no
@@ -571,7 +604,8 @@ __global__ void __launch_bounds__(BwdTc<D>::THREADS, 1)
       tma_store_commit();
       tma_store_wait_read();  // shared memory read out; the writes finish with the grid
     }
-  } else if (warp >= 8) {
+    }
+  } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ dQ
     const int c = ((warp & 3) << 5) + lane;  // head-dim index = TMEM lane
     const bool valid = c < D;                 // the same for the whole warp
@@ -839,10 +873,11 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT, LOSE>;
+  constexpr int threads = BwdEw<D, DROP>::THREADS;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, lse2, dvec, dq_acc,
+  kern<<<grid, threads, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, lse2, dvec, dq_acc,
                                           npad,
                                           static_cast<__nv_bfloat16*>(dk),
                                           static_cast<__nv_bfloat16*>(dv), split);

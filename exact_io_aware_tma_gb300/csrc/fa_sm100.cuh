@@ -407,6 +407,24 @@ __device__ __forceinline__ void mma_ts_mn_k64(uint32_t d, uint32_t a, uint64_t b
       : "memory");
 }
 
+// K = 64 (4 MMAs): A from TMEM in two 16-column halves 32 columns apart
+// (columns 0-15 and 32-47), B MN-major.
+__device__ __forceinline__ void mma_ts_mn_k64_gap32(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                      uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b32 a;\n .reg .b64 b;\n"
+      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " add.u32 a, %1, 8;\n add.s64 b, %2, 128;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 32;\n add.s64 b, %2, 256;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      " add.u32 a, %1, 40;\n add.s64 b, %2, 384;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
+      "}\n" ::"r"(d), "r"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
 // K = 64 (4 MMAs): A K-major within one 128-byte row, B MN-major.
 __device__ __forceinline__ void mma_ss_kmajor_mn_k64(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
                                       uint32_t acc) {
