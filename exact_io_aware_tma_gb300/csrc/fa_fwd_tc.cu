@@ -102,6 +102,111 @@ __device__ __forceinline__ bool live_bit(const uint32_t* live, int i, int first,
   return (live[i * kFwdLiveWords + (t >> 5)] >> (t & 31)) & 1u;
 }
 
+// One key tile of the online softmax for one query row (TMEM lane =
+// thread): S from TMEM columns col_s, the row's mask, the lazily moved
+// reference m_ref and the running sum l (O at col_o rescaled when the
+// reference moves and `rescale_o`), P as bf16 written back over S.  The
+// caller waits for the TMEM stores before signalling P.
+template <int D, bool DROP>
+__device__ __forceinline__ void softmax_tile(const Problem& p, long long bh, int row, int kt,
+                                             int klim, uint32_t lane_base, uint32_t col_s,
+                                             uint32_t col_o, bool rescale_o, float& m_ref,
+                                             float& l) {
+  const float cl2 = p.scale_log2;
+  float s[128];
+  {
+    uint32_t raw[128];
+    tmem_ld128(lane_base + col_s, raw);
+#pragma unroll
+    for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(raw[c]);
+  }
+  // This row's allowed keys in the tile: columns [lo, hi).  Masked
+  // scores get the value that the scale sends to -inf (and that the
+  // row max / min below ignores), so p = 2^-inf = 0 for either sign.
+  {
+    const int k0 = kt * 128;
+    const int lo = row_key_lo(p, row) - k0;
+    const int hi = row_key_hi(p, row, klim) + 1 - k0;
+    if (lo > 0 || hi < 128) {
+      const float fill = cl2 >= 0.f ? -INFINITY : INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c < lo || c >= hi) s[c] = fill;
+    }
+  }
+  // row max (row min for a negative scale): 4 independent chains of
+  // 3-input max
+  float mx;
+  if (cl2 >= 0.f) {
+    // s[0..3] seed the chains; 15 steps cover s[4..123]; s[124..127] last
+    float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+    for (int c = 4; c + 8 <= 124; c += 8)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m4[e] = max3f(m4[e], s[c + e], s[c + 4 + e]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m4[e] = fmaxf(m4[e], s[124 + e]);
+    mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+  } else {
+    float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+#pragma unroll
+    for (int c = 0; c < 128; ++c) m4[c & 3] = fminf(m4[c & 3], s[c]);
+    const float mn = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
+    mx = mn == INFINITY ? -INFINITY : mn;
+  }
+  const float m_tile = mx == -INFINITY ? -INFINITY : mx * cl2;
+  float alpha = 1.f;
+  if (m_tile > m_ref + 8.f) {
+    alpha = fast_exp2(m_ref - m_tile);  // 0 when m_ref = -inf
+    m_ref = m_tile;
+  }
+  const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
+  // p = 2^(s * scale*log2e - m): argument by packed FMA, exp2 on MUFU,
+  // row sum by packed adds over four independent pairs
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    // dropout: keep bits of the chunk's 32 keys (two generator calls of
+    // 16 keys each); dropped probabilities still count in the row sum
+    uint32_t keep = 0xffffffffu;
+    if constexpr (DROP) {
+      const uint4 a = dropout_bytes(p, bh, row, kt * 8 + 2 * c);
+      const uint4 b2 = dropout_bytes(p, bh, row, kt * 8 + 2 * c + 1);
+      keep = keep4(a.x, p.drop_p8) | keep4(a.y, p.drop_p8) << 4 |
+             keep4(a.z, p.drop_p8) << 8 | keep4(a.w, p.drop_p8) << 12 |
+             keep4(b2.x, p.drop_p8) << 16 | keep4(b2.y, p.drop_p8) << 20 |
+             keep4(b2.z, p.drop_p8) << 24 | keep4(b2.w, p.drop_p8) << 28;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float x0, x1;
+      fma2(x0, x1, s[32 * c + 2 * j], s[32 * c + 2 * j + 1], cl2, cl2, nref, nref);
+      const float p0 = fast_exp2(x0);
+      const float p1 = fast_exp2(x1);
+      add2(sa[j & 3], sb[j & 3], sa[j & 3], sb[j & 3], p0, p1);
+      if constexpr (DROP)
+        pk[j] = pack_bf16((keep >> (2 * j)) & 1u ? p0 : 0.f,
+                          (keep >> (2 * j + 1)) & 1u ? p1 : 0.f);
+      else
+        pk[j] = pack_bf16(p0, p1);
+    }
+    tmem_st16(lane_base + col_s + 16 * c, pk);
+  }
+  const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+  l = l * alpha + sum;
+  if (rescale_o && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(lane_base + col_o + 32 * c, o);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+      tmem_st32(lane_base + col_o + 32 * c, o);
+    }
+  }
+}
+
 // LOSE: self-test instantiation only (fa_selftest_forward_lost_signal): the
 // first softmax warp withholds its P-ready arrival for the first key tile
 // and every wait gives up after 1 ms, so the MMA issuer's wait runs out and
@@ -361,7 +466,6 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
       const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
       const uint32_t col_s = i == 0 ? C::COL_S0 : C::COL_S1;
       const uint32_t col_o = i == 0 ? C::COL_O0 : C::COL_O1;
-      const float cl2 = p.scale_log2;
       float m_ref = -INFINITY, l = 0.f;
       int n = 0;
       bool ok = true;
@@ -372,98 +476,7 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
         if (bmask ? !live_bit(live, i, ufirst, kt) : (kt < myfirst || kt > mylast)) continue;
         if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
         tc_fence_after();
-        float s[128];
-        {
-          uint32_t raw[128];
-          tmem_ld128(lane_base + col_s, raw);
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(raw[c]);
-        }
-        // This row's allowed keys in the tile: columns [lo, hi).  Masked
-        // scores get the value that the scale sends to -inf (and that the
-        // row max / min below ignores), so p = 2^-inf = 0 for either sign.
-        {
-          const int k0 = kt * 128;
-          const int lo = row_key_lo(p, row) - k0;
-          const int hi = row_key_hi(p, row, klim) + 1 - k0;
-          if (lo > 0 || hi < 128) {
-            const float fill = cl2 >= 0.f ? -INFINITY : INFINITY;
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c < lo || c >= hi) s[c] = fill;
-          }
-        }
-        // row max (row min for a negative scale): 4 independent chains of
-        // 3-input max
-        float mx;
-        if (cl2 >= 0.f) {
-          // s[0..3] seed the chains; 15 steps cover s[4..123]; s[124..127] last
-          float m4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-          for (int c = 4; c + 8 <= 124; c += 8)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) m4[e] = max3f(m4[e], s[c + e], s[c + 4 + e]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m4[e] = fmaxf(m4[e], s[124 + e]);
-          mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-        } else {
-          float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
-#pragma unroll
-          for (int c = 0; c < 128; ++c) m4[c & 3] = fminf(m4[c & 3], s[c]);
-          const float mn = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
-          mx = mn == INFINITY ? -INFINITY : mn;
-        }
-        const float m_tile = mx == -INFINITY ? -INFINITY : mx * cl2;
-        float alpha = 1.f;
-        if (m_tile > m_ref + 8.f) {
-          alpha = fast_exp2(m_ref - m_tile);  // 0 when m_ref = -inf
-          m_ref = m_tile;
-        }
-        const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
-        // p = 2^(s * scale*log2e - m): argument by packed FMA, exp2 on MUFU,
-        // row sum by packed adds over four independent pairs
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // dropout: keep bits of the chunk's 32 keys (two generator calls of
-          // 16 keys each); dropped probabilities still count in the row sum
-          uint32_t keep = 0xffffffffu;
-          if constexpr (DROP) {
-            const uint4 a = dropout_bytes(p, bh, row, kt * 8 + 2 * c);
-            const uint4 b2 = dropout_bytes(p, bh, row, kt * 8 + 2 * c + 1);
-            keep = keep4(a.x, p.drop_p8) | keep4(a.y, p.drop_p8) << 4 |
-                   keep4(a.z, p.drop_p8) << 8 | keep4(a.w, p.drop_p8) << 12 |
-                   keep4(b2.x, p.drop_p8) << 16 | keep4(b2.y, p.drop_p8) << 20 |
-                   keep4(b2.z, p.drop_p8) << 24 | keep4(b2.w, p.drop_p8) << 28;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float x0, x1;
-            fma2(x0, x1, s[32 * c + 2 * j], s[32 * c + 2 * j + 1], cl2, cl2, nref, nref);
-            const float p0 = fast_exp2(x0);
-            const float p1 = fast_exp2(x1);
-            add2(sa[j & 3], sb[j & 3], sa[j & 3], sb[j & 3], p0, p1);
-            if constexpr (DROP)
-              pk[j] = pack_bf16((keep >> (2 * j)) & 1u ? p0 : 0.f,
-                                (keep >> (2 * j + 1)) & 1u ? p1 : 0.f);
-            else
-              pk[j] = pack_bf16(p0, p1);
-          }
-          tmem_st16(lane_base + col_s + 16 * c, pk);
-        }
-        const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
-        l = l * alpha + sum;
-        if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + col_o + 32 * c, o);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(lane_base + col_o + 32 * c, o);
-          }
-        }
+        softmax_tile<D, DROP>(p, bh, row, kt, klim, lane_base, col_s, col_o, n > 0, m_ref, l);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
