@@ -468,58 +468,6 @@ __device__ __forceinline__ void mma_ss_mn_mn_k128(uint32_t d, uint64_t a, uint64
 }
 
 
-// ---- backward GEMM patterns with 128-query steps
-
-// K = 128 (8 MMAs): A from TMEM with its two 64-wide K halves 64 columns apart, B MN-major.
-__device__ __forceinline__ void mma_ts_split_mn_k128(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
-                                      uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p, t;\n .reg .b32 a;\n .reg .b64 b;\n"
-      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      " add.u32 a, %1, 8;\n add.s64 b, %2, 128;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      " add.u32 a, %1, 16;\n add.s64 b, %2, 256;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      " add.u32 a, %1, 24;\n add.s64 b, %2, 384;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      " add.u32 a, %1, 64;\n add.s64 b, %2, 512;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      " add.u32 a, %1, 72;\n add.s64 b, %2, 640;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      " add.u32 a, %1, 80;\n add.s64 b, %2, 768;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      " add.u32 a, %1, 88;\n add.s64 b, %2, 896;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n"
-      "}\n" ::"r"(d), "r"(a), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
-
-// K = 128 (8 MMAs): A K-major in 16 KB halves, B MN-major.
-__device__ __forceinline__ void mma_ss_kmajor_mn_k128(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                      uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p, t;\n .reg .b64 a, b;\n"
-      " setp.ne.b32 p, %4, 0;\n setp.eq.u32 t, 1, 1;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      " add.s64 a, %1, 2;\n add.s64 b, %2, 128;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      " add.s64 a, %1, 4;\n add.s64 b, %2, 256;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      " add.s64 a, %1, 6;\n add.s64 b, %2, 384;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      " add.s64 a, %1, 1024;\n add.s64 b, %2, 512;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      " add.s64 a, %1, 1026;\n add.s64 b, %2, 640;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      " add.s64 a, %1, 1028;\n add.s64 b, %2, 768;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      " add.s64 a, %1, 1030;\n add.s64 b, %2, 896;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n"
-      "}\n" ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
-
 // TMEM -> registers: 32 lanes x 32 consecutive 32-bit columns; thread t of
 // the warp receives lane (warp's lane base + t).  Waits for completion.
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
