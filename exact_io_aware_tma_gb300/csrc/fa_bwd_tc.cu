@@ -18,17 +18,23 @@
 //                                applies `scale`)
 // with D = rowsum(dO * O) and LSE*log2e precomputed per query row.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads; 512 at d = 64 without dropout):
 //   warp 0      TMA producer: K, V once; per step Q, dO (64 rows) and the
 //               64 LSE / D values into a ring of stages.
 //   warps 1, 2  MMA issuers (one thread each): warp 1 the recompute GEMMs
 //               S^T, dP^T (and owns TMEM), warp 2 the gradient GEMMs dV, dK,
 //               dQ^T.
 //   warps 4-7   element-wise: P^T, dS^T (one key row per thread); at the
-//               end dK, dV from TMEM to bf16 and a TMA store.
-//   warps 8-11  dQ: dQ^T from TMEM (one head-dim row per thread), added into
-//               the fp32 accumulator with red.global.add (coalesced across
-//               the warp), so the dQ tile costs no shared-memory traffic.
+//               end dK, dV from TMEM to bf16 and a TMA store.  At d = 64
+//               without dropout they take queries 0-31 of each step and
+//               warps 12-15 queries 32-63.
+//   warps 8-11  dQ: dQ^T from TMEM, one head-dim row per thread (warps whose
+//               lanes lie at or above d idle).  d = 128: added into the fp32
+//               accumulator with red.global.add from registers (coalesced
+//               across the warp), so the dQ tile costs no shared-memory
+//               traffic.  d = 64: each warp stages its 32 head dimensions
+//               of the step's 64 query rows in shared memory and adds them
+//               with one TMA reduce-add.
 //
 // TMEM columns: dV [0,d), dK [d,2d), S[b] = 2d + 64b, dP[b] = 2d + 128 + 64b
 // for the two step buffers b.  At d = 64 dQ^T has two buffers of its own,
