@@ -72,6 +72,13 @@ struct FwdTc {
   static_assert(SMEM <= (SOLO ? 232448 / 2 - 1024 : 232448), "shared memory budget");
   static constexpr int COL_S0 = 0, COL_S1 = 128, COL_O0 = SOLO ? 128 : 256, COL_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = SOLO ? 256 : 512;
+  // One-tile CTAs at d = 64 (SEPP): P has TMEM columns of its own (S 0-127,
+  // O 128-191, P 192-255), so S of the next key tile is computed as soon as
+  // the softmax has read this one into registers, while it still works on
+  // it.  The second tile's barriers serve as s_free (the softmax warps have
+  // read S) and p_free (the P . V that read P has completed).
+  static constexpr bool SEPP = SOLO && D == 64;  // used by the kernel without dropout
+  static constexpr int COL_P = 192, B_SFREE = B_S + 1, B_PFREE = B_P + 1;
 };
 
 // Next key tile after kt that is live for query tile q0 or q1, within the
@@ -105,13 +112,16 @@ __device__ __forceinline__ bool live_bit(const uint32_t* live, int i, int first,
 // One key tile of the online softmax for one query row (TMEM lane =
 // thread): S from TMEM columns col_s, the row's mask, the lazily moved
 // reference m_ref and the running sum l (O at col_o rescaled when the
-// reference moves and `rescale_o`), P as bf16 written back over S.  The
-// caller waits for the TMEM stores before signalling P.
-template <int D, bool DROP>
+// reference moves and `rescale_o`), P as bf16 written to columns col_p
+// (over S, or columns of its own).  after_load() runs once S is in
+// registers, before_store() before P or O is written.  The caller waits for
+// the TMEM stores before signalling P.
+template <int D, bool DROP, class AfterLoad, class BeforeStore>
 __device__ __forceinline__ void softmax_tile(const Problem& p, long long bh, int row, int kt,
                                              int klim, uint32_t lane_base, uint32_t col_s,
-                                             uint32_t col_o, bool rescale_o, float& m_ref,
-                                             float& l) {
+                                             uint32_t col_o, uint32_t col_p, bool rescale_o,
+                                             float& m_ref, float& l, AfterLoad after_load,
+                                             BeforeStore before_store) {
   const float cl2 = p.scale_log2;
   float s[128];
   {
@@ -120,6 +130,7 @@ __device__ __forceinline__ void softmax_tile(const Problem& p, long long bh, int
 #pragma unroll
     for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(raw[c]);
   }
+  after_load();
   // This row's allowed keys in the tile: columns [lo, hi).  Masked
   // scores get the value that the scale sends to -inf (and that the
   // row max / min below ignores), so p = 2^-inf = 0 for either sign.
@@ -161,6 +172,7 @@ __device__ __forceinline__ void softmax_tile(const Problem& p, long long bh, int
     m_ref = m_tile;
   }
   const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
+  before_store();
   // p = 2^(s * scale*log2e - m): argument by packed FMA, exp2 on MUFU,
   // row sum by packed adds over four independent pairs
   float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -191,7 +203,7 @@ __device__ __forceinline__ void softmax_tile(const Problem& p, long long bh, int
       else
         pk[j] = pack_bf16(p0, p1);
     }
-    tmem_st16(lane_base + col_s + 16 * c, pk);
+    tmem_st16(lane_base + col_p + 16 * c, pk);
   }
   const float sum = ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
   l = l * alpha + sum;
@@ -217,6 +229,9 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const Problem pin, float* __restrict__ lse, __nv_bfloat16* __restrict__ o_rows) {
   using C = FwdTc<D, SOLO>;
+  // P in columns of its own (one-tile CTAs at d = 64; with dropout the
+  // extra waits cost registers the Philox rounds need, so P stays over S)
+  constexpr bool SEPP = C::SEPP && !DROP;
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
   // (coordinates (x, h, start + row)), whose length then plays the role of N.
@@ -267,7 +282,9 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(bar(i), (i == C::B_P || i == C::B_P + 1) ? 4 : 1);
+      mbar_init(bar(i), (i == C::B_P || (i == C::B_P + 1 && !SEPP) || (i == C::B_SFREE && SEPP))
+                            ? 4
+                            : 1);
     *abort_flag = 0;
     fence_barrier_init();
     // the query tiles, issued by the producer thread before the rest of the
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
       int cur = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
-      int npv0 = 0, npv1 = 0;
+      int npv0 = 0, npv1 = 0, nsf = 0;
       if (ok && cur < p.T) {
         ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
         tc_fence_after();
@@ -422,6 +439,28 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
         if (!(ok = mbar_wait(bar(C::B_FULL + vslot), vphase, ab))) break;
         if (has_next && !(ok = mbar_wait(bar(C::B_FULL + kslot), kphase, ab))) break;
         tc_fence_after();
+        if constexpr (SEPP) {
+          // the next S as soon as the softmax has read this one (P has
+          // columns of its own), then P . V once P is ready
+          if (n0) {
+            if (!(ok = mbar_wait(bar(C::B_SFREE), nsf & 1, ab))) break;
+            ++nsf;
+            tc_fence_after();
+            qk(t_s0, dq0, kslot);
+            mma_commit(bar(C::B_S + 0));
+          }
+          if (l0) {
+            if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
+            tc_fence_after();
+            mma_ts_mn_k128(t_o0, tmem + C::COL_P, dv, id_pv, npv0 > 0);
+            mma_commit(bar(C::B_PFREE));
+            ++npv0;
+          }
+          mma_commit(bar(C::B_EMPTY + vslot));
+          if (has_next) mma_commit(bar(C::B_EMPTY + kslot));
+          cur = nxt;
+          continue;
+        }
         if (l0) {
           if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
           tc_fence_after();
@@ -476,7 +515,26 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
         if (bmask ? !live_bit(live, i, ufirst, kt) : (kt < myfirst || kt > mylast)) continue;
         if (!(ok = mbar_wait(bar(C::B_S + i), n & 1, ab))) break;
         tc_fence_after();
-        softmax_tile<D, DROP>(p, bh, row, kt, klim, lane_base, col_s, col_o, n > 0, m_ref, l);
+        // SEPP: S read -> the issuer may compute the next S into these
+        // columns; P and O are written only once the previous P . V (which
+        // read P and added into O) has completed
+        auto after_load = [&]() {
+          if constexpr (SEPP) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_SFREE));
+          }
+        };
+        auto before_store = [&]() {
+          if constexpr (SEPP) {
+            if (n > 0 && ok) ok = mbar_wait(bar(C::B_PFREE), (n - 1) & 1, ab);
+            tc_fence_after();
+          }
+        };
+        softmax_tile<D, DROP>(p, bh, row, kt, klim, lane_base, col_s, col_o,
+                              SEPP ? C::COL_P : col_s, n > 0, m_ref, l, after_load,
+                              before_store);
+        if (!ok) break;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
