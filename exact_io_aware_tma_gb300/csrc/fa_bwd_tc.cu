@@ -213,14 +213,18 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int klim = key_limit(p, b);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) {
+  if (warp == 0) {
+    // the barriers, one per lane of warp 0
+    for (int i = lane; i < C::NBAR; i += 32) {
       const bool ew = i == C::B_EW || i == C::B_EW + 1;
       const bool dqe = i == C::B_DQE || i == C::B_DQE + 1;
       mbar_init(bar(i), ew ? 4 * EW::GROUPS : dqe ? C::DQ_WARPS : 1);
     }
-    *abort_flag = 0;
     fence_barrier_init();
+    __syncwarp();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
     // K and V of the tile, issued by the producer thread before the rest of
     // the set-up (TMEM, the live bitmask, the CTA barrier) so that their
     // latency overlaps it

@@ -280,13 +280,17 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
   const int ufirst = first0 <= last0 ? first0 : first1;
   const int ulast = max(last0, last1);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i)
+  if (warp == 0) {
+    // the barriers, one per lane of warp 0
+    for (int i = lane; i < C::NBAR; i += 32)
       mbar_init(bar(i), (i == C::B_P || (i == C::B_P + 1 && !SEPP) || (i == C::B_SFREE && SEPP))
                             ? 4
                             : 1);
-    *abort_flag = 0;
     fence_barrier_init();
+    __syncwarp();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
     // the query tiles, issued by the producer thread before the rest of the
     // set-up (TMEM, the live bitmask, the CTA barrier) so that their latency
     // overlaps it
