@@ -189,6 +189,39 @@ def backward(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
     return dq, dk, dv
 
 
+class _Attention(torch.autograd.Function):
+    """Autograd node over ``forward`` / ``backward``: saves Q, K, V, O and the
+    LSE (no P: the backward rebuilds it), nothing else."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, block_mask, kv_len, window, dropout):
+        o, lse = forward(q, k, v, causal=causal, block_mask=block_mask, kv_len=kv_len,
+                         scale=scale, window=window, dropout=dropout)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.args = (causal, scale, block_mask, kv_len, window, dropout)
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        causal, scale, block_mask, kv_len, window, dropout = ctx.args
+        dq, dk, dv = backward(q, k, v, o, lse, do.contiguous(), causal=causal,
+                              block_mask=block_mask, kv_len=kv_len, scale=scale, window=window,
+                              dropout=dropout)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def attention(q, k, v, causal=False, scale=None, block_mask=None, kv_len=None, window=None,
+              dropout=None, return_lse=False):
+    """Differentiable exact attention: O = softmax(scale * Q K^T [masked]) V
+    for bf16 CUDA tensors [B, H, N, d], with the gradient of Q, K and V
+    computed by ``backward`` when autograd asks for it.  Arguments as in
+    ``forward``; returns O, or (O, LSE) with ``return_lse``."""
+    o, lse = _Attention.apply(q, k, v, causal, scale, block_mask, kv_len, window, dropout)
+    return (o, lse) if return_lse else o
+
+
 def backward_noalloc(q, k, v, o, lse, do, causal=False, block_mask=None, kv_len=None,
                      scale=None, dq=None, dk=None, dv=None, stream=None):
     """dQ, dK, dV like ``backward`` but with no workspace: the library's
