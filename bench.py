@@ -320,9 +320,13 @@ class Step:
         self.stream = stream
         self.launches = 6 if self.split else 4
 
-    def launch(self, ev):
-        """One step; ev[1], ev[2], ev[3] are recorded after the forward, the
-        preprocess and the dK/dV call (ev[0] / ev[4] belong to the caller)."""
+    def launch(self, ev, whole=False):
+        """One step; ev[1] is recorded after the forward (ev[0] / ev[4]
+        belong to the caller).  The backward is either its three calls with
+        ev[2], ev[3] recorded after the preprocess and the dK/dV call, or
+        (whole) the one fa_backward call, whose kernels may start while the
+        one before them finishes -- an event between two launches would end
+        that overlap."""
         from exact_io_aware_tma_gb300 import fa
         lib, P, t, st_ = self.lib, fa._ptr, self.t, self.stream
         sp = fa._stream(st_)
@@ -331,6 +335,13 @@ class Step:
         st = [lib.fa_forward(P(t["q"]), P(t["k"]), P(t["v"]), P(t["o"]), P(t["lse"]), B, H, N,
                              d, self.scale, self.causal, bmp, kvp, sp)]
         ev[1].record(st_)
+        if whole:
+            st.append(lib.fa_backward(P(t["q"]), P(t["k"]), P(t["v"]), P(t["o"]), P(t["lse"]),
+                                      P(t["do"]), P(t["dq"]), P(t["dk"]), P(t["dv"]), B, H, N, d,
+                                      self.scale, self.causal, bmp, kvp, ws, wsb, sp))
+            if st[-1] != 0 or st[0] != 0:
+                raise RuntimeError(f"library call failed: {[fa.status_string(s) for s in st]}")
+            return
         st.append(lib.fa_backward_preprocess(P(t["o"]), P(t["do"]), P(t["lse"]), B, H, N, d, ws,
                                              wsb, sp))
         ev[2].record(st_)
@@ -346,11 +357,14 @@ class Step:
 def time_workload_table(steps, warmup, dev, flush, min_seconds=0.4):
     """Forward and backward TFLOP/s of every workload of the method's list
     (tiny, BERT key padding, GPT-2 causal, long-context causal, block
-    sparse), each timed like the headline step: L2 flushed before every step
-    (outside the events), CUDA events around each launch on the launching
-    stream.  A workload runs at least `steps` timed steps and keeps going
-    (in rounds of `steps`) until `min_seconds` of wall time have passed, so
-    the SM clock sampler sees it under load; every timed step counts."""
+    sparse): L2 flushed before every step (outside the events), CUDA events
+    on the launching stream around the forward call and around the one
+    fa_backward call.  A workload runs at least `steps` timed steps and keeps
+    going (in rounds of `steps`) until `min_seconds` of wall time have
+    passed, so the SM clock sampler sees it under load; every timed step
+    counts.  The backward's per-call split (preprocess, dK/dV, dQ
+    conversion) comes from a second pass of `steps` steps that makes the
+    three calls with events between them."""
     import numpy as np
     import torch
     from exact_io_aware_tma_gb300 import fa
@@ -375,16 +389,25 @@ def time_workload_table(steps, warmup, dev, flush, min_seconds=0.4):
                 for ev in evs:
                     flush.zero_()
                     ev[0].record(stream)
-                    step.launch(ev)
+                    step.launch(ev, whole=True)
                     ev[4].record(stream)
                 torch.cuda.synchronize()
-                segs += [[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in evs]
+                segs += [[ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[4])] for ev in evs]
                 n += steps
+        parts = []
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for ev in evs:
+            flush.zero_()
+            ev[0].record(stream)
+            step.launch(ev)
+            ev[4].record(stream)
+        torch.cuda.synchronize()
+        parts = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(1, 4)] for ev in evs])
         if fa.last_device_status(stream) != 0:
             raise RuntimeError(f"{name}: device status not OK")
         seg = np.array(segs)
         fwd_ms = float(seg[:, 0].mean())
-        bwd_ms = float(seg[:, 1:].sum(axis=1).mean())
+        bwd_ms = float(seg[:, 1].mean())
         f_fwd, f_bwd = flops(cfg, dense_fraction(cfg))
         fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
         bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
@@ -392,9 +415,10 @@ def time_workload_table(steps, warmup, dev, flush, min_seconds=0.4):
             "B": cfg["B"], "H": cfg["H"], "N": cfg["N"], "d": cfg["d"], "mask": cfg["mask"],
             "fwd_gflop": f_fwd / 1e9, "bwd_gflop": f_bwd / 1e9,
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-            "bwd_kernel_ms": {"preprocess": float(seg[:, 1].mean()),
-                              "dkdv": float(seg[:, 2].mean()),
-                              "dq_convert": float(seg[:, 3].mean())},
+            "bwd_calls_ms": {"preprocess": float(parts[:, 0].mean()),
+                             "dkdv": float(parts[:, 1].mean()),
+                             "dq_convert": float(parts[:, 2].mean()),
+                             "note": "separate pass, events between the three calls"},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "pct_of_measured_peak": {"fwd": 100 * fwd_tf / peak, "bwd": 100 * bwd_tf / peak},
             "pct_of_datasheet_peak": {"fwd": 100 * fwd_tf / DATASHEET_BF16_TFLOPS,

@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256)
                           float* __restrict__ dq_acc, long long heads, int N, int npad) {
   constexpr int CH = D / 8;
   const long long n = heads * npad * CH;
+  griddep_wait();
+  griddep_release();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n;
        i += (long long)gridDim.x * blockDim.x) {
     float acc = 0.f;
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(256)
   constexpr int CH = D / 8;
   const long long n = heads * npad * CH;
   const long long stride = (long long)gridDim.x * blockDim.x;
+  griddep_wait();
+  griddep_release();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n;
        i += stride) {
     float acc = 0.f;
@@ -134,6 +138,8 @@ __global__ void __launch_bounds__(256)
     dq_convert_packed_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                              float scale, int H, int total, int d) {
   const long long chunks = (long long)total * H * (d / 8);
+  griddep_wait();
+  griddep_release();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
        i += (long long)gridDim.x * blockDim.x) {
     const long long e = i * 8;  // element of dq [total][H][d]
@@ -157,6 +163,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     dq_convert_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                       float scale, long long chunks) {
+  griddep_wait();
+  griddep_release();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
        i += (long long)gridDim.x * blockDim.x) {
     float4 a = reinterpret_cast<const float4*>(dq_acc + i * 8)[0];
@@ -395,48 +403,59 @@ int fa_backward_preprocess(const void* o, const void* dout, const float* lse, in
   const unsigned nblk = elementwise_blocks(heads * npad * (d / 8));
   auto ob = static_cast<const __nv_bfloat16*>(o);
   auto db = static_cast<const __nv_bfloat16*>(dout);
-  if (d == 64)
-    bwd_preprocess_kernel<64><<<nblk, 256, 0, s>>>(ob, db, lse, ws_lse2(workspace),
-                                                   ws_dvec(workspace, heads, N),
-                                                   ws_dq_acc(workspace, heads, N), heads, N, npad);
-  else
-    bwd_preprocess_kernel<128><<<nblk, 256, 0, s>>>(ob, db, lse, ws_lse2(workspace),
-                                                    ws_dvec(workspace, heads, N),
-                                                    ws_dq_acc(workspace, heads, N), heads, N, npad);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e = launch_k(
+      true, d == 64 ? bwd_preprocess_kernel<64> : bwd_preprocess_kernel<128>, dim3(nblk),
+      dim3(256), 0, s, ob, db, lse, ws_lse2(workspace), ws_dvec(workspace, heads, N),
+      ws_dq_acc(workspace, heads, N), heads, N, npad);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-static int backward_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
-                         void* dv, int B, int H, int N, int d, float scale, const fa_mask* mask,
-                         void* workspace, size_t workspace_bytes, void* stream) {
-  Problem p;
-  int st = check_sizes(B, H, N, d, scale, mask, &p);
+// The dK/dV call's problem and, with a block mask and room for the split's
+// extra workspace, its split (key tiles with many live query tiles spread
+// over several CTAs).
+static int dkdv_problem(const void* q, const void* k, const void* v, const void* dout,
+                        const void* dk, const void* dv, int B, int H, int N, int d, float scale,
+                        const fa_mask* mask, void* workspace, size_t workspace_bytes,
+                        Problem* p, BwdSplit* split, bool* use_split) {
+  int st = check_sizes(B, H, N, d, scale, mask, p);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !dout || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) ||
-      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(p.kv_len, 4))
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(p->kv_len, 4))
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
-  p.status = status_word();
-  if (p.status == nullptr) return FA_ERR_CUDA;
-  const long long heads = (long long)B * H;
-  // Block mask and room for the split's extra workspace: key tiles with many
-  // live query tiles are spread over several CTAs.
-  BwdSplit split{};
-  const size_t base = fa_backward_workspace_bytes(B, H, N, d), extra = split_bytes(p);
-  const bool use_split = extra != 0 && workspace_bytes >= base + extra;
-  if (use_split) {
+  p->status = status_word();
+  if (p->status == nullptr) return FA_ERR_CUDA;
+  *split = BwdSplit{};
+  const size_t base = fa_backward_workspace_bytes(B, H, N, d), extra = split_bytes(*p);
+  *use_split = extra != 0 && workspace_bytes >= base + extra;
+  if (*use_split) {
     char* w = static_cast<char*>(workspace) + base;
-    split.items = reinterpret_cast<const int4*>(w);
-    w += round_up((size_t)p.T * kSplitMax * sizeof(int4), 256);
-    split.nitems = reinterpret_cast<const int*>(w);
+    split->items = reinterpret_cast<const int4*>(w);
+    w += round_up((size_t)p->T * kSplitMax * sizeof(int4), 256);
+    split->nitems = reinterpret_cast<const int*>(w);
     w += 256;
-    split.slots = reinterpret_cast<float*>(w);
+    split->slots = reinterpret_cast<float*>(w);
   }
+  return FA_OK;
+}
+
+// early: called straight after the preprocess's launch, with the split's
+// plan (if any) launched before that preprocess.
+static int backward_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                         void* dv, int B, int H, int N, int d, float scale, const fa_mask* mask,
+                         void* workspace, size_t workspace_bytes, void* stream, bool early) {
+  Problem p;
+  BwdSplit split;
+  bool use_split;
+  int st = dkdv_problem(q, k, v, dout, dk, dv, B, H, N, d, scale, mask, workspace,
+                        workspace_bytes, &p, &split, &use_split);
+  if (st != FA_OK) return st;
+  const long long heads = (long long)B * H;
   cudaError_t e = launch_bwd_tc(p, q, k, v, dout, ws_lse2(workspace),
                                 ws_dvec(workspace, heads, N), ws_dq_acc(workspace, heads, N),
-                                dk, dv, padded_rows(N), use_split ? &split : nullptr,
+                                dk, dv, padded_rows(N), use_split ? &split : nullptr, early,
                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -447,7 +466,7 @@ int fa_backward_dkdv(const void* q, const void* k, const void* v, const void* do
                      size_t workspace_bytes, void* stream) {
   const fa_mask m = plain_mask(causal, block_mask, kv_len);
   return backward_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, &m, workspace, workspace_bytes,
-                       stream);
+                       stream, false);
 }
 
 int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
@@ -460,10 +479,11 @@ int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float scale,
   if (st != FA_OK) return st;
   const long long heads = (long long)B * H;
   const long long chunks = heads * N * (d / 8);
-  dq_convert_kernel<<<elementwise_blocks(chunks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      ws_dq_acc(const_cast<void*>(workspace), heads, N), static_cast<__nv_bfloat16*>(dq), scale,
-      chunks);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e =
+      launch_k(true, dq_convert_kernel, dim3(elementwise_blocks(chunks)), dim3(256), 0,
+               static_cast<cudaStream_t>(stream), ws_dq_acc(const_cast<void*>(workspace), heads, N),
+               static_cast<__nv_bfloat16*>(dq), scale, chunks);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_backward_masked(const void* q, const void* k, const void* v, const void* o,
@@ -482,10 +502,22 @@ int fa_backward_masked(const void* q, const void* k, const void* v, const void* 
     return FA_ERR_INVALID_ARG;
   st = check_workspace(B, H, N, d, workspace, workspace_bytes);
   if (st != FA_OK) return st;
+  // The split's plan (block mask) goes first and the preprocess waits for
+  // it, so the dK/dV kernel can start while the preprocess runs.
+  {
+    Problem pd;
+    BwdSplit split;
+    bool use_split;
+    st = dkdv_problem(q, k, v, dout, dk, dv, B, H, N, d, scale, mask, workspace, workspace_bytes,
+                      &pd, &split, &use_split);
+    if (st != FA_OK) return st;
+    if (use_split && launch_bwd_plan(pd, split, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
   st = fa_backward_preprocess(o, dout, lse, B, H, N, d, workspace, workspace_bytes, stream);
   if (st != FA_OK) return st;
   st = backward_dkdv(q, k, v, dout, dk, dv, B, H, N, d, scale, mask, workspace, workspace_bytes,
-                     stream);
+                     stream, true);
   if (st != FA_OK) return st;
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }
@@ -591,21 +623,17 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
   const unsigned nblk = elementwise_blocks(heads * npad * (d / 8));
   auto ob = static_cast<const __nv_bfloat16*>(o);
   auto db = static_cast<const __nv_bfloat16*>(dout);
-  if (d == 64)
-    bwd_preprocess_packed_kernel<64><<<nblk, 256, 0, s>>>(ob, db, lse, lse2, dvec, dq_acc,
-                                                          cu_seqlens, H, heads, total,
-                                                          max_seqlen, npad);
-  else
-    bwd_preprocess_packed_kernel<128><<<nblk, 256, 0, s>>>(ob, db, lse, lse2, dvec, dq_acc,
-                                                           cu_seqlens, H, heads, total,
-                                                           max_seqlen, npad);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  cudaError_t e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, nullptr, s);
+  cudaError_t e = launch_k(
+      true, d == 64 ? bwd_preprocess_packed_kernel<64> : bwd_preprocess_packed_kernel<128>,
+      dim3(nblk), dim3(256), 0, s, ob, db, lse, lse2, dvec, dq_acc, cu_seqlens, H, heads, total,
+      max_seqlen, npad);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, nullptr, true, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   const long long chunks = (long long)total * H * (d / 8);
-  dq_convert_packed_kernel<<<elementwise_blocks(chunks), 256, 0, s>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), scale, H, total, d);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  e = launch_k(true, dq_convert_packed_kernel, dim3(elementwise_blocks(chunks)), dim3(256), 0, s,
+               (const float*)dq_acc, static_cast<__nv_bfloat16*>(dq), scale, H, total, d);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_selftest_forward_lost_signal(const void* q, const void* k, const void* v, void* o,

@@ -271,6 +271,9 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // the preprocess's LSE and D rows are read from here on
+      griddep_wait();
+      griddep_release();
       int qt = -1, sub = 0, slot = 0, round = 0;
       while (next_q_step<D>(p, kt, klim, smem, qt, sub)) {
         const int q0 = qt * 128 + sub * 64;
@@ -627,6 +630,7 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int qt = -1, sub = 0;
     bool ok = true;
+    if (valid) griddep_wait();  // the accumulator the preprocess cleared
     for (int i = 0; valid && next_q_step<D>(p, kt, klim, smem, qt, sub); ++i) {
       const int bf = i & 1;
       const int q0 = qt * 128 + sub * 64;
@@ -713,6 +717,8 @@ __global__ void __launch_bounds__(1024)
   __shared__ int slots, next_base, nsplit;
   const int T = p.T, tid = threadIdx.x, nth = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
+  griddep_wait();
+  griddep_release();
   if (tid == 0) {
     tot = 0;
     next_base = 0;
@@ -813,6 +819,8 @@ __global__ void __launch_bounds__(256)
                           const float* __restrict__ slots, __nv_bfloat16* __restrict__ dk,
                           __nv_bfloat16* __restrict__ dv) {
   const int j = blockIdx.x;
+  griddep_wait();
+  griddep_release();
   if (j >= __ldg(plan + 1)) return;
   const int kt = __ldg(plan + 2 + 3 * j), base = __ldg(plan + 3 + 3 * j),
             n = __ldg(plan + 4 + 3 * j);
@@ -842,11 +850,28 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+cudaError_t launch_bwd_plan(const Problem& p, const BwdSplit& split, cudaStream_t st) {
+  // the current device's SM count, asked on every call (a few hundred
+  // nanoseconds; a process-wide cache would be wrong across devices and
+  // racy across host threads)
+  int dev = 0, nsm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  return launch_k(true, bwd_plan_kernel, dim3(1), dim3(1024), 0, st, p, nsm,
+                  (long long)p.B * p.H, const_cast<int4*>(split.items),
+                  const_cast<int*>(split.nitems));
+}
+
+// early: launched straight after the preprocess kernel, which waited for the
+// split plan (launched before it); the kernel may then start while the
+// preprocess is still running.
 template <int D, bool PACKED, bool DROP, bool SPLIT, bool LOSE = false>
 static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void* k,
                                    const void* v, const void* dout, const float* lse2,
                                    const float* dvec, float* dq_acc, void* dk, void* dv, int npad,
-                                   const BwdSplit& split, cudaStream_t st) {
+                                   const BwdSplit& split, bool early, cudaStream_t st) {
   using C = BwdTc<D>;
   // Heads per CTA group: Q, dO (bf16) and the fp32 dQ accumulator of a group
   // within about 64 MB (half of L2).
@@ -876,45 +901,37 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
   if (!maps) return cudaErrorInvalidValue;
   cudaError_t e;
   if constexpr (SPLIT) {
-    // the current device's SM count, asked on every call (a few hundred
-    // nanoseconds; a process-wide cache would be wrong across devices and
-    // racy across host threads)
-    int dev = 0, nsm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
-    bwd_plan_kernel<<<1, 1024, 0, st>>>(p, nsm, bh, const_cast<int4*>(split.items),
-                                        const_cast<int*>(split.nitems));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!early && (e = launch_bwd_plan(p, split, st)) != cudaSuccess) return e;
   }
   auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT, LOSE>;
   constexpr int threads = BwdEw<D, DROP>::THREADS;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
-  kern<<<grid, threads, C::SMEM, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, lse2, dvec, dq_acc,
-                                          npad,
-                                          static_cast<__nv_bfloat16*>(dk),
-                                          static_cast<__nv_bfloat16*>(dv), split);
+  e = launch_k(early, kern, grid, dim3(threads), C::SMEM, st, tq, tk, tv, tdo, tdk, tdv, tdq, p,
+               lse2, dvec, dq_acc, npad, static_cast<__nv_bfloat16*>(dk),
+               static_cast<__nv_bfloat16*>(dv), split);
   if constexpr (SPLIT) {
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     dim3 jgrid(kSplitSlots / 2, (unsigned)(bh < 65535 ? bh : 65535));
-    bwd_split_join_kernel<D><<<jgrid, 256, 0, st>>>(p, bh, split.nitems, split.slots,
-                                                    static_cast<__nv_bfloat16*>(dk),
-                                                    static_cast<__nv_bfloat16*>(dv));
+    e = launch_k(true, bwd_split_join_kernel<D>, jgrid, dim3(256), 0, st, p, bh,
+                 (const int*)split.nitems, (const float*)split.slots,
+                 static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv));
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <bool PACKED, bool DROP, bool SPLIT>
 static cudaError_t launch_bwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
                                    const void* dout, const float* lse2, const float* dvec,
                                    float* dq_acc, void* dk, void* dv, int npad,
-                                   const BwdSplit& split, cudaStream_t st) {
+                                   const BwdSplit& split, bool early, cudaStream_t st) {
   return p.d == 64 ? launch_bwd_tc_t<64, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
-                                                              dq_acc, dk, dv, npad, split, st)
+                                                              dq_acc, dk, dv, npad, split, early,
+                                                              st)
                    : launch_bwd_tc_t<128, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
-                                                               dq_acc, dk, dv, npad, split, st);
+                                                               dq_acc, dk, dv, npad, split,
+                                                               early, st);
 }
 
 cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
@@ -924,28 +941,29 @@ cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const voi
   if (p.d != 128 || p.cu_seqlens != nullptr || p.drop_p8 != 0) return cudaErrorInvalidValue;
   const BwdSplit none{nullptr, nullptr, nullptr};
   return launch_bwd_tc_t<128, false, false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc,
-                                                         dk, dv, npad, none, st);
+                                                         dk, dv, npad, none, false, st);
 }
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
-                          void* dk, void* dv, int npad, const BwdSplit* split, cudaStream_t st) {
+                          void* dk, void* dv, int npad, const BwdSplit* split, bool early,
+                          cudaStream_t st) {
   const bool packed = p.cu_seqlens != nullptr, drop = p.drop_p8 != 0;
   const BwdSplit none{nullptr, nullptr, nullptr};
   if (packed)
     return drop ? launch_bwd_tc_d<true, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                     npad, none, st)
+                                                     npad, none, early, st)
                 : launch_bwd_tc_d<true, false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
-                                                      dv, npad, none, st);
+                                                      dv, npad, none, early, st);
   if (split != nullptr)
     return drop ? launch_bwd_tc_d<false, true, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                     npad, *split, st)
+                                                     npad, *split, early, st)
                 : launch_bwd_tc_d<false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
-                                                      dv, npad, *split, st);
+                                                      dv, npad, *split, early, st);
   return drop ? launch_bwd_tc_d<false, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                    npad, none, st)
+                                                    npad, none, early, st)
               : launch_bwd_tc_d<false, false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                     npad, none, st);
+                                                     npad, none, early, st);
 }
 
 }  // namespace fa

@@ -217,6 +217,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute may start while the kernel before it in the
+// stream is still running; griddep_wait() returns once that kernel has
+// completed and its writes are visible (at once for a kernel launched the
+// ordinary way).  griddep_release() lets the next kernel so launched be
+// scheduled.  Every kernel here releases only after its own wait, so a kernel
+// that starts early still finds all work before its predecessor complete:
+// only what the predecessor itself writes needs the wait.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

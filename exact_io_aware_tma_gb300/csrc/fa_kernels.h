@@ -7,6 +7,25 @@
 
 namespace fa {
 
+// Launch of `kern` on `st`; with `early`, the programmatic stream-serialisation
+// attribute lets it start before the previous kernel in the stream ends (the
+// kernel then calls griddep_wait() before it touches that kernel's output).
+template <class... Params, class... Args>
+cudaError_t launch_k(bool early, void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = early ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+}
+
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           void* o, float* lse, cudaStream_t st);
 
@@ -14,10 +33,15 @@ int* status_word();
 
 // split != nullptr (padded layout with a block mask): the work of key tiles
 // with many live query tiles is spread over several CTAs by a plan kernel
-// launched first (BwdSplit in fa_common.cuh).
+// (BwdSplit in fa_common.cuh), launched first unless `early`.  early: the
+// call comes straight after the preprocess kernel's launch, and the plan (for
+// a split) was launched before that preprocess; the dK/dV kernel may then
+// start while the preprocess runs.
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
-                          void* dk, void* dv, int npad, const BwdSplit* split, cudaStream_t st);
+                          void* dk, void* dv, int npad, const BwdSplit* split, bool early,
+                          cudaStream_t st);
+cudaError_t launch_bwd_plan(const Problem& p, const BwdSplit& split, cudaStream_t st);
 
 // Self-test launches of the d = 128 forward (tile-pair CTAs) and dK/dV
 // kernels in which one warp withholds one arrival and waits give up after

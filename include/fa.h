@@ -169,9 +169,15 @@ FA_API size_t fa_backward_workspace_bytes_masked(int B, int H, int N, int d,
  *                256-byte aligned, owned by the caller; its contents on
  *                entry are ignored and on exit are unspecified.
  *   Other arguments as in fa_forward and equal to the forward call's.
+ *   dq, dk, dv and the workspace must not overlap each other or any input.
  * Launches, in order on `stream`: the D = rowsum(dO * O) preprocess (which
  * also clears the dQ accumulator), the dK/dV kernel (which also adds each
- * tile's dS K into the dQ accumulator), and the dQ conversion.
+ * tile's dS K into the dQ accumulator), and the dQ conversion; with a split
+ * (below), its plan kernel first.  Each kernel after the first is launched
+ * with programmatic dependent launch: it may start, and do the set-up that
+ * needs no result of the kernel before it, while that kernel finishes; it
+ * waits for that kernel's results before it reads them.  No kernel starts
+ * before all work enqueued ahead of the call has completed.
  */
 FA_API int fa_backward(const void* q, const void* k, const void* v, const void* o,
                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
@@ -189,8 +195,11 @@ FA_API int fa_backward_masked(const void* q, const void* k, const void* v, const
 /*
  * The three launches of fa_backward, exposed one by one so a caller can
  * time or overlap them; calling them in this order on one stream with the
- * same workspace is exactly fa_backward.  Arguments mean what they mean in
- * fa_backward; each validates its own arguments.
+ * same workspace computes exactly what fa_backward computes (fa_backward
+ * also starts the dK/dV kernel's set-up during the preprocess's tail, which
+ * the separate calls do not).  Arguments mean what they mean in
+ * fa_backward; each validates its own arguments and none reads memory that
+ * work enqueued ahead of it may still be writing.
  *
  * fa_backward_preprocess: D = rowsum(dO * O) and LSE*log2(e) into the
  *   workspace (padding rows and rows without an allowed key get +inf, so
