@@ -28,11 +28,13 @@ __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                           const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
                           float* __restrict__ lse2, float* __restrict__ dvec,
-                          float* __restrict__ dq_acc, long long heads, int N, int npad) {
+                          float* __restrict__ dq_acc, unsigned long long* __restrict__ next_item,
+                          long long heads, int N, int npad) {
   constexpr int CH = D / 8;
   const long long n = heads * npad * CH;
   griddep_wait();
   griddep_release();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *next_item = 0;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n;
        i += (long long)gridDim.x * blockDim.x) {
     float acc = 0.f;
@@ -342,7 +344,8 @@ size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
   Problem p;
   if (check_sizes(B, H, N, d, 1.0f, nullptr, &p) != FA_OK) return 0;
   const size_t vec = round_up((size_t)B * H * padded_rows(N) * sizeof(float), 256);
-  return 2 * vec + round_up((size_t)B * H * N * d * sizeof(float), 256);
+  // LSE*log2(e), D, the fp32 dQ accumulator, the dK/dV kernel's work counter
+  return 2 * vec + round_up((size_t)B * H * N * d * sizeof(float), 256) + 256;
 }
 
 // Extra workspace of the split backward (block masks): the plan's items and
@@ -380,6 +383,12 @@ static float* ws_dvec(void* ws, long long heads, int N) {
 static float* ws_dq_acc(void* ws, long long heads, int N) {
   return reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ws_vec_bytes(heads, N));
 }
+// work-item counter of the persistent dK/dV kernel (cleared by the preprocess)
+static unsigned long long* ws_counter(void* ws, long long heads, int N, int d) {
+  return reinterpret_cast<unsigned long long*>(
+      static_cast<char*>(ws) + 2 * ws_vec_bytes(heads, N) +
+      round_up((size_t)heads * N * d * sizeof(float), 256));
+}
 
 // Elementwise kernels: enough CTAs for every chunk, capped at a few waves.
 static unsigned elementwise_blocks(long long chunks) {
@@ -406,7 +415,7 @@ int fa_backward_preprocess(const void* o, const void* dout, const float* lse, in
   const cudaError_t e = launch_k(
       true, d == 64 ? bwd_preprocess_kernel<64> : bwd_preprocess_kernel<128>, dim3(nblk),
       dim3(256), 0, s, ob, db, lse, ws_lse2(workspace), ws_dvec(workspace, heads, N),
-      ws_dq_acc(workspace, heads, N), heads, N, npad);
+      ws_dq_acc(workspace, heads, N), ws_counter(workspace, heads, N, d), heads, N, npad);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -455,7 +464,8 @@ static int backward_dkdv(const void* q, const void* k, const void* v, const void
   const long long heads = (long long)B * H;
   cudaError_t e = launch_bwd_tc(p, q, k, v, dout, ws_lse2(workspace),
                                 ws_dvec(workspace, heads, N), ws_dq_acc(workspace, heads, N),
-                                dk, dv, padded_rows(N), use_split ? &split : nullptr, early,
+                                dk, dv, padded_rows(N), use_split ? &split : nullptr,
+                                ws_counter(workspace, heads, N, d), early,
                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -628,7 +638,8 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
       dim3(nblk), dim3(256), 0, s, ob, db, lse, lse2, dvec, dq_acc, cu_seqlens, H, heads, total,
       max_seqlen, npad);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, nullptr, true, s);
+  e = launch_bwd_tc(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, nullptr, nullptr, true,
+                    s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   const long long chunks = (long long)total * H * (d / 8);
   e = launch_k(true, dq_convert_packed_kernel, dim3(elementwise_blocks(chunks)), dim3(256), 0, s,

@@ -871,7 +871,8 @@ template <int D, bool PACKED, bool DROP, bool SPLIT, bool LOSE = false>
 static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void* k,
                                    const void* v, const void* dout, const float* lse2,
                                    const float* dvec, float* dq_acc, void* dk, void* dv, int npad,
-                                   const BwdSplit& split, bool early, cudaStream_t st) {
+                                   const BwdSplit& split, unsigned long long* next_item,
+                                   bool early, cudaStream_t st) {
   using C = BwdTc<D>;
   // Heads per CTA group: Q, dO (bf16) and the fp32 dQ accumulator of a group
   // within about 64 MB (half of L2).
@@ -882,35 +883,43 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
     p.hgroup = (int)(g < 1 ? 1 : (g > heads ? heads : g));
   }
   const long long bh = (long long)p.B * p.H;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-  bool maps;
-  if constexpr (PACKED)
-    maps = make_bf16_map_packed(&tq, q, D, p.H, p.total, C::BQ) &&
-           make_bf16_map_packed(&tk, k, D, p.H, p.total, 128) &&
-           make_bf16_map_packed(&tv, v, D, p.H, p.total, 128) &&
-           make_bf16_map_packed(&tdo, dout, D, p.H, p.total, C::BQ) &&
-           make_bf16_map_packed(&tdk, dk, D, p.H, p.total, 128) &&
-           make_bf16_map_packed(&tdv, dv, D, p.H, p.total, 128) &&
-           make_f32_map_3d(&tdq, dq_acc, D, p.total, p.H, C::BQ, 32);
-  else
-    maps = make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) &&
-           make_bf16_map_3d(&tk, k, D, p.N, bh, 128) && make_bf16_map_3d(&tv, v, D, p.N, bh, 128) &&
-           make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) &&
-           make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) && make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128) &&
-           make_f32_map_3d(&tdq, dq_acc, D, p.N, bh, C::BQ, 32);
-  if (!maps) return cudaErrorInvalidValue;
   cudaError_t e;
   if constexpr (SPLIT) {
     if (!early && (e = launch_bwd_plan(p, split, st)) != cudaSuccess) return e;
   }
-  auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT, LOSE>;
-  constexpr int threads = BwdEw<D, DROP>::THREADS;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
-  e = launch_k(early, kern, grid, dim3(threads), C::SMEM, st, tq, tk, tv, tdo, tdk, tdv, tdq, p,
-               lse2, dvec, dq_acc, npad, static_cast<__nv_bfloat16*>(dk),
-               static_cast<__nv_bfloat16*>(dv), split);
+  if constexpr (D == 64 && !PACKED && !DROP && !LOSE) {
+    // d = 64: the persistent kernel (fa_bwd_persist.cu)
+    e = launch_bwd_persist(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad,
+                           SPLIT ? &split : nullptr, next_item, early, st);
+  } else {
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+    bool maps;
+    if constexpr (PACKED)
+      maps = make_bf16_map_packed(&tq, q, D, p.H, p.total, C::BQ) &&
+             make_bf16_map_packed(&tk, k, D, p.H, p.total, 128) &&
+             make_bf16_map_packed(&tv, v, D, p.H, p.total, 128) &&
+             make_bf16_map_packed(&tdo, dout, D, p.H, p.total, C::BQ) &&
+             make_bf16_map_packed(&tdk, dk, D, p.H, p.total, 128) &&
+             make_bf16_map_packed(&tdv, dv, D, p.H, p.total, 128) &&
+             make_f32_map_3d(&tdq, dq_acc, D, p.total, p.H, C::BQ, 32);
+    else
+      maps = make_bf16_map_3d(&tq, q, D, p.N, bh, C::BQ) &&
+             make_bf16_map_3d(&tk, k, D, p.N, bh, 128) &&
+             make_bf16_map_3d(&tv, v, D, p.N, bh, 128) &&
+             make_bf16_map_3d(&tdo, dout, D, p.N, bh, C::BQ) &&
+             make_bf16_map_3d(&tdk, dk, D, p.N, bh, 128) &&
+             make_bf16_map_3d(&tdv, dv, D, p.N, bh, 128) &&
+             make_f32_map_3d(&tdq, dq_acc, D, p.N, bh, C::BQ, 32);
+    if (!maps) return cudaErrorInvalidValue;
+    auto kern = bwd_tc_kernel<D, PACKED, DROP, SPLIT, LOSE>;
+    constexpr int threads = BwdEw<D, DROP>::THREADS;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(bh * p.T * (SPLIT ? kSplitMax : 1)));
+    e = launch_k(early, kern, grid, dim3(threads), C::SMEM, st, tq, tk, tv, tdo, tdk, tdv, tdq, p,
+                 lse2, dvec, dq_acc, npad, static_cast<__nv_bfloat16*>(dk),
+                 static_cast<__nv_bfloat16*>(dv), split);
+  }
   if constexpr (SPLIT) {
     if (e != cudaSuccess) return e;
     dim3 jgrid(kSplitSlots / 2, (unsigned)(bh < 65535 ? bh : 65535));
@@ -925,13 +934,14 @@ template <bool PACKED, bool DROP, bool SPLIT>
 static cudaError_t launch_bwd_tc_d(const Problem& p, const void* q, const void* k, const void* v,
                                    const void* dout, const float* lse2, const float* dvec,
                                    float* dq_acc, void* dk, void* dv, int npad,
-                                   const BwdSplit& split, bool early, cudaStream_t st) {
+                                   const BwdSplit& split, unsigned long long* next_item,
+                                   bool early, cudaStream_t st) {
   return p.d == 64 ? launch_bwd_tc_t<64, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
-                                                              dq_acc, dk, dv, npad, split, early,
-                                                              st)
+                                                              dq_acc, dk, dv, npad, split,
+                                                              next_item, early, st)
                    : launch_bwd_tc_t<128, PACKED, DROP, SPLIT>(p, q, k, v, dout, lse2, dvec,
                                                                dq_acc, dk, dv, npad, split,
-                                                               early, st);
+                                                               next_item, early, st);
 }
 
 cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
@@ -941,29 +951,30 @@ cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const voi
   if (p.d != 128 || p.cu_seqlens != nullptr || p.drop_p8 != 0) return cudaErrorInvalidValue;
   const BwdSplit none{nullptr, nullptr, nullptr};
   return launch_bwd_tc_t<128, false, false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc,
-                                                         dk, dv, npad, none, false, st);
+                                                         dk, dv, npad, none, nullptr, false,
+                                                         st);
 }
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
-                          void* dk, void* dv, int npad, const BwdSplit* split, bool early,
-                          cudaStream_t st) {
+                          void* dk, void* dv, int npad, const BwdSplit* split,
+                          unsigned long long* next_item, bool early, cudaStream_t st) {
   const bool packed = p.cu_seqlens != nullptr, drop = p.drop_p8 != 0;
   const BwdSplit none{nullptr, nullptr, nullptr};
   if (packed)
     return drop ? launch_bwd_tc_d<true, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                     npad, none, early, st)
+                                                     npad, none, next_item, early, st)
                 : launch_bwd_tc_d<true, false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
-                                                      dv, npad, none, early, st);
+                                                      dv, npad, none, next_item, early, st);
   if (split != nullptr)
     return drop ? launch_bwd_tc_d<false, true, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                     npad, *split, early, st)
+                                                     npad, *split, next_item, early, st)
                 : launch_bwd_tc_d<false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc, dk,
-                                                      dv, npad, *split, early, st);
+                                                      dv, npad, *split, next_item, early, st);
   return drop ? launch_bwd_tc_d<false, true, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                    npad, none, early, st)
+                                                    npad, none, next_item, early, st)
               : launch_bwd_tc_d<false, false, false>(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv,
-                                                     npad, none, early, st);
+                                                     npad, none, next_item, early, st);
 }
 
 }  // namespace fa

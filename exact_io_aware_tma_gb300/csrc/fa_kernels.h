@@ -36,12 +36,23 @@ int* status_word();
 // (BwdSplit in fa_common.cuh), launched first unless `early`.  early: the
 // call comes straight after the preprocess kernel's launch, and the plan (for
 // a split) was launched before that preprocess; the dK/dV kernel may then
-// start while the preprocess runs.
+// start while the preprocess runs.  next_item: the work-item counter of the
+// persistent d = 64 kernel (padded layout, no dropout), cleared by the
+// preprocess; nullptr for the other forms.
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse2, const float* dvec, float* dq_acc,
-                          void* dk, void* dv, int npad, const BwdSplit* split, bool early,
-                          cudaStream_t st);
+                          void* dk, void* dv, int npad, const BwdSplit* split,
+                          unsigned long long* next_item, bool early, cudaStream_t st);
 cudaError_t launch_bwd_plan(const Problem& p, const BwdSplit& split, cudaStream_t st);
+
+// The persistent dK/dV kernel of d = 64 (padded layout, no dropout): one CTA
+// per SM taking work items from `next_item` (cleared by the preprocess).
+// p.hgroup set by the caller; split: the plan's items, or nullptr.
+cudaError_t launch_bwd_persist(const Problem& p, const void* q, const void* k, const void* v,
+                               const void* dout, const float* lse2, const float* dvec,
+                               float* dq_acc, void* dk, void* dv, int npad,
+                               const BwdSplit* split, unsigned long long* next_item, bool early,
+                               cudaStream_t st);
 
 // Self-test launches of the d = 128 forward (tile-pair CTAs) and dK/dV
 // kernels in which one warp withholds one arrival and waits give up after

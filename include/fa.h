@@ -134,7 +134,8 @@ FA_API int fa_forward_masked(const void* q, const void* k, const void* v, void* 
 /*
  * Bytes of device workspace fa_backward needs: LSE*log2(e) and D
  * (fp32 [B*H][Np] each, Np = N rounded up to a multiple of 128) followed by
- * the fp32 dQ accumulator [B,H,N,d], each part 256-byte aligned.
+ * the fp32 dQ accumulator [B,H,N,d] and 256 bytes for the dK/dV kernel's
+ * work-item counter, each part 256-byte aligned.
  * O(B*H*N*d): linear in N (no N x N buffer).  Returns 0 for invalid sizes.
  */
 FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
@@ -207,8 +208,9 @@ FA_API int fa_backward_masked(const void* q, const void* k, const void* v, const
  *   accumulator [B,H,N,d].
  * fa_backward_dkdv: for every live 128-key tile, recomputes P and dS from
  *   Q, K, V, dO and the workspace's LSE and D, writes dK (times scale) and
- *   dV, and adds dS K into the workspace's dQ accumulator.  Needs the
- *   preprocess first.  With a block mask and a workspace of
+ *   dV, and adds dS K into the workspace's dQ accumulator.  Needs its own
+ *   preprocess call first (which also resets the work counter it takes its
+ *   key tiles from at d = 64).  With a block mask and a workspace of
  *   fa_backward_workspace_bytes_masked() it is three launches (the split
  *   plan, the kernel, the join of the split key tiles).
  * fa_backward_dq_convert: dQ = scale * accumulator, rounded to bf16.
@@ -240,7 +242,7 @@ FA_API int fa_backward_dq_convert(void* dq, int B, int H, int N, int d, float sc
  * library and held until the process exits.  Nothing is allocated.
  *  - Problems whose fa_backward_workspace_bytes() exceeds
  *    FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_INVALID_ARG before
- *    any CUDA call.  That size is 2 * r(4*B*H*Np) + r(4*B*H*N*d) bytes,
+ *    any CUDA call.  That size is 2 * r(4*B*H*Np) + r(4*B*H*N*d) + 256 bytes,
  *    with Np = N rounded up to a multiple of 128 and r() rounding up to a
  *    multiple of 256; call fa_backward_workspace_bytes() to test a shape
  *    (e.g. B*H = 16, N = 8192, d = 64 needs 33.0 MiB and is rejected; at

@@ -51,12 +51,13 @@ def test_status_strings(lib):
 
 def test_workspace_is_linear_in_n(lib):
     # LSE*log2e and D (fp32 per row, rows padded to 128 per head) + fp32 dQ
-    # accumulator, each rounded to 256 bytes: no N x N term (the backward
-    # needs O(N) extra memory per head).
+    # accumulator, each rounded to 256 bytes, + 256 bytes for the dK/dV
+    # kernel's work counter: no N x N term (the backward needs O(N) extra
+    # memory per head).
     f = lib.fa_backward_workspace_bytes
     for B, H, N, d in [(1, 1, 128, 64), (2, 16, 8192, 128), (1, 8, 16384, 64), (3, 5, 7, 64)]:
         prow = B * H * (-(-N // 128) * 128)
-        want = 2 * (-(-prow * 4 // 256) * 256) + -(-B * H * N * d * 4 // 256) * 256
+        want = 2 * (-(-prow * 4 // 256) * 256) + -(-B * H * N * d * 4 // 256) * 256 + 256
         assert f(B, H, N, d) == want
     assert f(0, 1, 128, 64) == 0 and f(1, 1, 128, 96) == 0
 
