@@ -673,7 +673,7 @@ int fa_selftest_backward_lost_signal(const void* q, const void* k, const void* v
   Problem p;
   int st = check_sizes(B, H, N, d, scale, &m, &p);
   if (st != FA_OK) return st;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 128 && d != 64) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
@@ -688,7 +688,8 @@ int fa_selftest_backward_lost_signal(const void* q, const void* k, const void* v
   const long long heads = (long long)B * H;
   cudaError_t e = launch_bwd_tc_lost_signal(
       p, q, k, v, dout, ws_lse2(workspace), ws_dvec(workspace, heads, N),
-      ws_dq_acc(workspace, heads, N), dk, dv, padded_rows(N), static_cast<cudaStream_t>(stream));
+      ws_dq_acc(workspace, heads, N), dk, dv, padded_rows(N), ws_counter(workspace, heads, N, d),
+      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return FA_ERR_CUDA;
   return fa_backward_dq_convert(dq, B, H, N, d, scale, workspace, workspace_bytes, stream);
 }

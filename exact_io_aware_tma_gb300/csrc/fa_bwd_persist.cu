@@ -156,7 +156,11 @@ __device__ __forceinline__ bool next_step(const Problem& p, int kt, int klim,
   return false;
 }
 
-template <bool SPLIT>
+// LOSE: self-test instantiation only (fa_selftest_backward_lost_signal at
+// d = 64): warp 4 withholds its arrival for the CTA's first step and every
+// wait gives up after 1 ms, so the gradient issuer's wait runs out and the
+// abort, drain and status paths run.
+template <bool SPLIT, bool LOSE = false>
 __global__ void __launch_bounds__(PTc::THREADS, 1)
     bwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
   volatile PItem* info = reinterpret_cast<volatile PItem*>(smem + C::OFF_MISC + 64);
-  const Abort ab{abort_flag, p.status, kWaitLimitNs};
+  const Abort ab{abort_flag, p.status, LOSE ? kShortWaitLimitNs : kWaitLimitNs};
   // item n's live bitmask and K/V buffer
   auto live_of = [&](int n) {
     return reinterpret_cast<const uint32_t*>(smem + C::OFF_LIVE + (n & 1) * C::LIVEB);
@@ -543,7 +547,7 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_EW + bf));
+        if (lane == 0 && !(LOSE && s == 0 && warp == 4)) mbar_arrive(bar(C::B_EW + bf));
       }
       if (g == 0) {
         // ---- epilogue: dK (x scale), dV out of TMEM; a part of a split key
@@ -690,7 +694,7 @@ cudaError_t launch_bwd_persist(const Problem& p, const void* q, const void* k, c
                                const void* dout, const float* lse2, const float* dvec,
                                float* dq_acc, void* dk, void* dv, int npad,
                                const BwdSplit* split, unsigned long long* next_item, bool early,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool lose) {
   if (p.d != 64 || p.cu_seqlens != nullptr || p.drop_p8 != 0 || next_item == nullptr)
     return cudaErrorInvalidValue;
   const long long bh = (long long)p.B * p.H;
@@ -711,7 +715,9 @@ cudaError_t launch_bwd_persist(const Problem& p, const void* q, const void* k, c
   long long ctas = bh * p.T * (split != nullptr ? kSplitMax : 1);
   if (ctas > nsm) ctas = nsm;
   const BwdSplit none{nullptr, nullptr, nullptr};
-  auto kern = split != nullptr ? bwd_persist_kernel<true> : bwd_persist_kernel<false>;
+  auto kern = lose ? bwd_persist_kernel<false, true>
+                   : split != nullptr ? bwd_persist_kernel<true> : bwd_persist_kernel<false>;
+  if (lose && split != nullptr) return cudaErrorInvalidValue;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PTc::SMEM)) !=
       cudaSuccess)
     return e;

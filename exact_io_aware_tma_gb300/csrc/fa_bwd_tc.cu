@@ -887,10 +887,10 @@ static cudaError_t launch_bwd_tc_t(const Problem& pin, const void* q, const void
   if constexpr (SPLIT) {
     if (!early && (e = launch_bwd_plan(p, split, st)) != cudaSuccess) return e;
   }
-  if constexpr (D == 64 && !PACKED && !DROP && !LOSE) {
+  if constexpr (D == 64 && !PACKED && !DROP) {
     // d = 64: the persistent kernel (fa_bwd_persist.cu)
     e = launch_bwd_persist(p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad,
-                           SPLIT ? &split : nullptr, next_item, early, st);
+                           SPLIT ? &split : nullptr, next_item, early, st, LOSE);
   } else {
     CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     bool maps;
@@ -947,12 +947,16 @@ static cudaError_t launch_bwd_tc_d(const Problem& p, const void* q, const void* 
 cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
                                       const void* v, const void* dout, const float* lse2,
                                       const float* dvec, float* dq_acc, void* dk, void* dv,
-                                      int npad, cudaStream_t st) {
-  if (p.d != 128 || p.cu_seqlens != nullptr || p.drop_p8 != 0) return cudaErrorInvalidValue;
+                                      int npad, unsigned long long* next_item, cudaStream_t st) {
+  if ((p.d != 128 && p.d != 64) || p.cu_seqlens != nullptr || p.drop_p8 != 0)
+    return cudaErrorInvalidValue;
   const BwdSplit none{nullptr, nullptr, nullptr};
-  return launch_bwd_tc_t<128, false, false, false, true>(p, q, k, v, dout, lse2, dvec, dq_acc,
-                                                         dk, dv, npad, none, nullptr, false,
-                                                         st);
+  return p.d == 128 ? launch_bwd_tc_t<128, false, false, false, true>(
+                          p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, none, nullptr,
+                          false, st)
+                    : launch_bwd_tc_t<64, false, false, false, true>(
+                          p, q, k, v, dout, lse2, dvec, dq_acc, dk, dv, npad, none, next_item,
+                          false, st);
 }
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,

@@ -47,23 +47,25 @@ cudaError_t launch_bwd_plan(const Problem& p, const BwdSplit& split, cudaStream_
 
 // The persistent dK/dV kernel of d = 64 (padded layout, no dropout): one CTA
 // per SM taking work items from `next_item` (cleared by the preprocess).
-// p.hgroup set by the caller; split: the plan's items, or nullptr.
+// p.hgroup set by the caller; split: the plan's items, or nullptr.  lose:
+// the self-test instantiation that withholds one arrival (no split).
 cudaError_t launch_bwd_persist(const Problem& p, const void* q, const void* k, const void* v,
                                const void* dout, const float* lse2, const float* dvec,
                                float* dq_acc, void* dk, void* dv, int npad,
                                const BwdSplit* split, unsigned long long* next_item, bool early,
-                               cudaStream_t st);
+                               cudaStream_t st, bool lose = false);
 
-// Self-test launches of the d = 128 forward (tile-pair CTAs) and dK/dV
-// kernels in which one warp withholds one arrival and waits give up after
-// 1 ms: the bounded-wait abort path, reached on purpose (padded layout, no
-// dropout; cudaErrorInvalidValue otherwise).
+// Self-test launches of the d = 128 forward (tile-pair CTAs) and of the
+// dK/dV kernels (d = 128, and the persistent d = 64 kernel, which takes the
+// workspace's work counter) in which one warp withholds one arrival and
+// waits give up after 1 ms: the bounded-wait abort path, reached on purpose
+// (padded layout, no dropout; cudaErrorInvalidValue otherwise).
 cudaError_t launch_fwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
                                       const void* v, void* o, float* lse, cudaStream_t st);
 cudaError_t launch_bwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
                                       const void* v, const void* dout, const float* lse2,
                                       const float* dvec, float* dq_acc, void* dk, void* dv,
-                                      int npad, cudaStream_t st);
+                                      int npad, unsigned long long* next_item, cudaStream_t st);
 
 // e4m3 forward (d = 128) on quantised operands: q8, k8 [B*H][N][128],
 // vt8 [B*H][128][ceil(N/128)*128], q/k scales [B*H][T], v scale [B*H].
