@@ -4,7 +4,8 @@ dependent launch) and wait for that kernel's results before it reads them.
 Calls queued back to back on one stream, sharing one workspace, must each
 see their own preprocess (LSE, D, the cleared dQ accumulator) and their own
 split plan: the results must equal those of the same calls made one at a
-time with the stream drained in between.  Marked ``gpu``."""
+time with the stream drained in between.  A backward captured in a CUDA
+graph keeps that order on every replay.  Marked ``gpu``."""
 
 import pytest
 import torch
@@ -85,3 +86,42 @@ def test_back_to_back_packed_calls_see_their_own_preprocess():
         ref = wq.float().abs().max().item()
         assert (dq.float() - wq.float()).abs().max().item() <= 1e-2 * ref, i
     assert not torch.equal(want[0][1], want[1][1])
+
+
+@pytest.mark.parametrize("d,mask", [(64, "causal"), (128, "causal"), (64, "band_global")])
+def test_backward_captured_in_a_cuda_graph(d, mask):
+    # the backward's kernels carry the programmatic-launch attribute; a
+    # stream capture keeps those edges, and replays give the eager results
+    extra = dict(global_every=4) if mask == "band_global" else {}
+    inp = make_inputs(B=1, H=4, N=1024, d=d, mask=mask, seed=60 + d, **extra)
+    g = to_device(inp)
+    kw = dict(causal=g["causal"], block_mask=g["block_mask"], scale=g["scale"])
+    B, H, N, _ = g["q"].shape
+    o, lse = fa.forward(g["q"], g["k"], g["v"], **kw)
+    ws = torch.empty(fa.backward_workspace_bytes(B, H, N, d, g["block_mask"]), device="cuda",
+                     dtype=torch.uint8)
+    dq, dk, dv = (torch.empty_like(g["q"]) for _ in range(3))
+    do = g["do"].clone()
+    torch.cuda.synchronize()
+    want = [t.clone() for t in fa.backward(g["q"], g["k"], g["v"], o, lse, do, workspace=ws, **kw)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            fa.backward(g["q"], g["k"], g["v"], o, lse, do, workspace=ws, dq=dq, dk=dk, dv=dv,
+                        stream=s, **kw)
+    torch.cuda.synchronize()
+    for scale in (1.0, -0.5):
+        do.copy_((g["do"].float() * scale).to(do.dtype))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fa.last_device_status() == fa.FA_OK
+        ref = [t.clone() for t in fa.backward(g["q"], g["k"], g["v"], o, lse, do, **kw)]
+        torch.cuda.synchronize()
+        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+        top = ref[0].float().abs().max().item()
+        assert (dq.float() - ref[0].float()).abs().max().item() <= 1e-2 * top
+        # the replay read the new dO
+        assert torch.equal(dk, want[1]) == (scale == 1.0)
