@@ -5,7 +5,9 @@
 // key limit; dead tiles are never loaded) through a ring of shared-memory
 // slots filled by TMA.  The SOLO instantiation owns one query tile (warps 2-5
 // do its softmax, TMEM columns S [0,128), O [128,128+d)) and runs two CTAs
-// per SM.  The online-softmax recurrence of page
+// per SM; at d = 64 it keeps P in columns of its own and its ring is two
+// stages of {V_j, K_(j+1)} (one full and one empty barrier per key tile).
+// The online-softmax recurrence of page
 // "FlashAttention" (aiwiki), section "Tiling and online normalization", is
 // evaluated per query row in log2 units with a lazily moved reference:
 //     m' = max over the tile of scale*log2(e)*q.k_j
@@ -333,7 +335,107 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (SEPP && warp <= 1) {
+    // One-tile d = 64 CTAs: the ring is two stages of two slots, stage t
+    // holding V of the t-th live key tile and K of the next one (slots 2s
+    // and 2s + 1, s = t mod 2) on one full and one empty barrier, so that a
+    // key tile costs the issuer one load wait and one release.  K of the
+    // first tile goes to slot 3 ahead of stage 1.
+    constexpr uint32_t slot_step = C::TILE >> 4;  // descriptor units per ring slot
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      bool ok = true;
+      int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
+      int t = 0;  // stages issued
+      const int first_k = kt < p.T ? 1 : 0;
+      if (first_k) {
+        mbar_expect_tx(bar(C::B_FULL + 1), C::TILE);
+        tma_load_3d(s0 + C::OFF_KV + 3 * C::TILE, &tm_k, bar(C::B_FULL + 1), 0, cy(kt * 128),
+                    cz(kt * 128));
+      }
+      while (ok && kt < p.T) {
+        const int nxt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt);
+        const int s = t & 1;
+        // stage t reuses the slots of stage t - 2, released by the issuer
+        // after key tile t - 2; stage 1 waits for the first S instead (slot 3)
+        if (t >= 1 &&
+            !(ok = mbar_wait(bar(C::B_EMPTY + s), ((t - 1) >> 1) & 1, ab, kSleepHintNs)))
+          break;
+        const uint32_t fb = bar(C::B_FULL + s);
+        mbar_expect_tx(fb, (nxt < p.T ? 2 : 1) * C::TILE);
+        tma_load_3d(s0 + C::OFF_KV + 2 * s * C::TILE, &tm_v, fb, 0, cy(kt * 128), cz(kt * 128));
+        if (nxt < p.T)
+          tma_load_3d(s0 + C::OFF_KV + (2 * s + 1) * C::TILE, &tm_k, fb, 0, cy(nxt * 128),
+                      cz(nxt * 128));
+        ++t;
+        kt = nxt;
+      }
+      // Drain (matters only after an abort): the last phase issued on each
+      // full barrier -- stages 0, 2, ... on barrier 0; the first K and
+      // stages 1, 3, ... on barrier 1 -- and the query tile.
+      const int nphase[2] = {(t + 1) >> 1, first_k + (t >> 1)};
+      for (int b2 = 0; b2 < 2; ++b2) {
+        if (nphase[b2] == 0) continue;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar(C::B_FULL + b2), (nphase[b2] - 1) & 1) &&
+               globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+      {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar(C::B_Q), 0) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
+      const uint64_t dq = sdesc_sw128(s0 + C::OFF_Q, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(s0 + C::OFF_KV, 16, 1024);      // K operand of slot 0
+      const uint64_t dv0 = sdesc_sw128(s0 + C::OFF_KV, C::HALF, 1024);  // V operand of slot 0
+      const uint32_t t_s = tmem + C::COL_S0, t_o = tmem + C::COL_O0, t_p = tmem + C::COL_P;
+      bool ok = mbar_wait(bar(C::B_Q), 0, ab);
+      tc_fence_after();
+      int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
+      if (ok && kt < p.T) {
+        ok = mbar_wait(bar(C::B_FULL + 1), 0, ab);
+        tc_fence_after();
+        if (ok) {
+          mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)(3 * slot_step), id_qk, 0);
+          mma_commit(bar(C::B_S));
+          mma_commit(bar(C::B_EMPTY + 1));
+        }
+      }
+      for (int j = 0; ok && kt < p.T; ++j) {
+        const int nxt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt);
+        const int s = j & 1;
+        // stage j is phase j / 2 of full barrier 0 (j even) or phase
+        // (j + 1) / 2 of full barrier 1 (j odd, after the first K)
+        if (!(ok = mbar_wait(bar(C::B_FULL + s), ((j + s) >> 1) & 1, ab))) break;
+        tc_fence_after();
+        if (nxt < p.T) {
+          // the next S as soon as the softmax has read this one (P has
+          // columns of its own)
+          if (!(ok = mbar_wait(bar(C::B_SFREE), j & 1, ab))) break;
+          tc_fence_after();
+          mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)((2 * s + 1) * slot_step), id_qk, 0);
+          mma_commit(bar(C::B_S));
+        }
+        if (!(ok = mbar_wait(bar(C::B_P), j & 1, ab))) break;
+        tc_fence_after();
+        mma_ts_mn_k128(t_o, t_p, dv0 + (uint64_t)(2 * s * slot_step), id_pv, j > 0);
+        mma_commit(bar(C::B_PFREE));
+        mma_commit(bar(C::B_EMPTY + s));
+        kt = nxt;
+      }
+      mma_commit(bar(C::B_O));
+      // Drain all issued tensor-core work before TMEM can be released.
+      mma_commit(bar(C::B_DRAIN));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int slot = 0, round = 0;
@@ -411,7 +513,7 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
       int cur = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
-      int npv0 = 0, npv1 = 0, nsf = 0;
+      int npv0 = 0, npv1 = 0;
       if (ok && cur < p.T) {
         ok = mbar_wait(bar(C::B_FULL + slot), phase, ab);
         tc_fence_after();
@@ -443,28 +545,6 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
         if (!(ok = mbar_wait(bar(C::B_FULL + vslot), vphase, ab))) break;
         if (has_next && !(ok = mbar_wait(bar(C::B_FULL + kslot), kphase, ab))) break;
         tc_fence_after();
-        if constexpr (SEPP) {
-          // the next S as soon as the softmax has read this one (P has
-          // columns of its own), then P . V once P is ready
-          if (n0) {
-            if (!(ok = mbar_wait(bar(C::B_SFREE), nsf & 1, ab))) break;
-            ++nsf;
-            tc_fence_after();
-            qk(t_s0, dq0, kslot);
-            mma_commit(bar(C::B_S + 0));
-          }
-          if (l0) {
-            if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
-            tc_fence_after();
-            mma_ts_mn_k128(t_o0, tmem + C::COL_P, dv, id_pv, npv0 > 0);
-            mma_commit(bar(C::B_PFREE));
-            ++npv0;
-          }
-          mma_commit(bar(C::B_EMPTY + vslot));
-          if (has_next) mma_commit(bar(C::B_EMPTY + kslot));
-          cur = nxt;
-          continue;
-        }
         if (l0) {
           if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
           tc_fence_after();
