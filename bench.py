@@ -264,9 +264,10 @@ def run_reference_kvcache(args, name):
 
 # ---------------------------------------------------------------- GPU arm
 
-def traffic_record(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
-    kernel source has not changed since the capture; else None."""
+def traffic_record(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if that summary holds a capture of this kernel on this workload
+    and the kernel source has not changed since; else None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
@@ -279,7 +280,7 @@ def traffic_record(kernel):
         kv = dict(x.split("=", 1) for x in line.split())
         recs[kv.get("kernel")] = kv
     r = recs.get(kernel)
-    if r is None:
+    if r is None or r.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "exact_io_aware_tma_gb300", "csrc", r["source"])
     if not os.path.exists(src):
@@ -635,7 +636,7 @@ def run_gpu(args, cfg, name):
                           "bwd_dq_convert": conv_ms},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_kind": peak_kind, "traffic": traffic_record(dom)},
+                         "peak_kind": peak_kind, "traffic": traffic_record(dom, name)},
             "cpu_baseline": cpu_base,
             "e2e": e2e,
             "gpu_launches": (6 if split else 4) * args.steps,
