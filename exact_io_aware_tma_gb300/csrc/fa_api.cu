@@ -654,7 +654,7 @@ int fa_selftest_forward_lost_signal(const void* q, const void* k, const void* v,
   Problem p;
   int st = check_sizes(B, H, N, d, scale, &m, &p);
   if (st != FA_OK) return st;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 128 && d != 64) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;

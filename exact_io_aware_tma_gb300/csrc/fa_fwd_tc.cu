@@ -759,7 +759,10 @@ static cudaError_t launch_fwd_tc_d(const Problem& p, const void* q, const void* 
 
 cudaError_t launch_fwd_tc_lost_signal(const Problem& p, const void* q, const void* k,
                                       const void* v, void* o, float* lse, cudaStream_t st) {
-  if (p.d != 128 || p.cu_seqlens != nullptr || p.drop_p8 != 0) return cudaErrorInvalidValue;
+  if ((p.d != 128 && p.d != 64) || p.cu_seqlens != nullptr || p.drop_p8 != 0)
+    return cudaErrorInvalidValue;
+  // d = 64: the one-tile kernel (P apart, two-stage ring)
+  if (p.d == 64) return launch_fwd_tc_t<64, false, false, true, true>(p, q, k, v, o, lse, st);
   return launch_fwd_tc_t<128, false, false, false, true>(p, q, k, v, o, lse, st);
 }
 

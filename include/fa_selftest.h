@@ -52,9 +52,10 @@ FA_API int fa_selftest_mma(int mode, const void* a, const void* b, float* c, int
  * flight finish (again with bounded waits), frees its tensor memory and
  * exits, so a lost signal cannot hang the GPU.  These two entry points run
  * that path on purpose: the same arguments as fa_forward / fa_backward (no
- * block mask or key lengths; d = 128 for the forward, d = 128 or 64 for the
- * backward, whose d = 64 kernel is the persistent one; FA_ERR_UNSUPPORTED
- * for other d), but one warp of each CTA withholds one arrival (the
+ * block mask or key lengths; d = 128 or 64, the forward's d = 64 kernel
+ * being the one-query-tile one with P in TMEM columns of its own and the
+ * backward's the persistent one; FA_ERR_UNSUPPORTED for other d), but one
+ * warp of each CTA withholds one arrival (the
  * forward's first softmax warp its P-ready signal for its first key tile;
  * the backward's first element-wise warp its signal for the CTA's first
  * query step) and the waits give up after 1 ms instead of 2 s.  The call returns FA_OK at

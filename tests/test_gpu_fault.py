@@ -48,10 +48,13 @@ def run_lost_signal(which, g, B, H, N, d):
     return st
 
 
-@pytest.mark.parametrize("which,d", [("forward", 128), ("backward", 128), ("backward", 64)])
+@pytest.mark.parametrize("which,d", [("forward", 128), ("forward", 64), ("backward", 128),
+                                     ("backward", 64)])
 def test_withheld_arrival_times_out_and_the_device_stays_usable(which, d):
-    # d = 64: more work items (B*H*T = 192) than persistent CTAs (one per
-    # SM), so the CTAs abort with items still to fetch
+    # backward d = 64: more work items (B*H*T = 192) than persistent CTAs
+    # (one per SM), so the CTAs abort with items still to fetch; forward
+    # d = 64: two one-tile CTAs per SM, each aborting with the next S issued
+    # and its stage loads in flight
     B, H, N = (1, 4, 1024) if d == 128 else (2, 12, 1024)
     inp = make_inputs(B=B, H=H, N=N, d=d, mask="causal", seed=41)
     g = to_device(inp)
@@ -85,9 +88,9 @@ def test_withheld_arrival_times_out_and_the_device_stays_usable(which, d):
 
 def test_lost_signal_entry_points_reject_other_head_dims():
     lib = fa.load()
-    x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(1, 1, 128, 96, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(1, 1, 128, dtype=torch.float32, device="cuda")
     P = fa._ptr
-    st = lib.fa_selftest_forward_lost_signal(P(x), P(x), P(x), P(x), P(lse), 1, 1, 128, 64,
+    st = lib.fa_selftest_forward_lost_signal(P(x), P(x), P(x), P(x), P(lse), 1, 1, 128, 96,
                                              0.125, 1, fa._stream())
     assert st == fa.FA_ERR_UNSUPPORTED
