@@ -3,10 +3,11 @@
 // One CTA owns two 128-row query tiles of one (b, h) (tiles 2p and 2p+1) and
 // streams the union of their live 128-key tiles (block mask, causal rule,
 // key limit; dead tiles are never loaded) through a ring of shared-memory
-// slots filled by TMA.  The SOLO instantiation owns one query tile (warps 2-5
-// do its softmax, TMEM columns S [0,128), O [128,128+d)) and runs two CTAs
-// per SM; at d = 64 it keeps P in columns of its own and its ring is two
-// stages of {V_j, K_(j+1)} (one full and one empty barrier per key tile).
+// slots filled by TMA, in stages of {V_j, K_(j+1)} (one full and one empty
+// barrier per key tile).  The SOLO instantiation owns one query tile (warps
+// 2-5 do its softmax, TMEM columns S [0,128), O [128,128+d)) and runs two
+// CTAs per SM; at d = 64 it keeps P in columns of its own, otherwise (P over
+// S) its ring is of single K and V tiles.
 // The online-softmax recurrence of page
 // "FlashAttention" (aiwiki), section "Tiling and online normalization", is
 // evaluated per query row in log2 units with a lazily moved reference:
@@ -19,7 +20,7 @@
 // rounding; it saves most rescalings of the accumulator.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: Q tiles once, then K_j, V_j into the slot ring.
+//   warp 0      TMA producer: Q tiles once, then V_j and K_(j+1) into a stage.
 //   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T into TMEM, then
 //               O_i += P_i V_j with P_i read from TMEM; owns TMEM.
 //   warps 4-7   softmax for query tile 0 (TMEM lanes 0-127, one row per thread)
@@ -62,8 +63,9 @@ struct FwdTc {
   static constexpr int OFF_Q = 0;                // Q0, Q1 (reused for O staging)
   static constexpr int OFF_KV = NQ * TILE;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
-  // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_ready[2],
-  // o_done[2], drain
+  // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT] (one per slot, or
+  // one per stage of two slots in the staged ring, which uses the first
+  // NSLOT / 2 of each), s_full[2], p_ready[2], o_done[2], drain
   static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_S = 1 + 2 * NSLOT,
                        B_P = B_S + 2, B_O = B_P + 2, B_DRAIN = B_O + 2, NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -234,6 +236,8 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
   // P in columns of its own (one-tile CTAs at d = 64; with dropout the
   // extra waits cost registers the Philox rounds need, so P stays over S)
   constexpr bool SEPP = C::SEPP && !DROP;
+  // the staged K/V ring (below) everywhere but the one-tile kernel with P over S
+  constexpr bool STAGED = SEPP || !SOLO;
   // Geometry of this CTA's (b, h): padded layout [B*H][N][d] (TMA coordinates
   // (x, row, bh)), or one sequence of the packed layout [total][H][d]
   // (coordinates (x, h, start + row)), whose length then plays the role of N.
@@ -335,49 +339,55 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (SEPP && warp <= 1) {
-    // One-tile d = 64 CTAs: the ring is two stages of two slots, stage t
-    // holding V of the t-th live key tile and K of the next one (slots 2s
-    // and 2s + 1, s = t mod 2) on one full and one empty barrier, so that a
-    // key tile costs the issuer one load wait and one release.  K of the
-    // first tile goes to slot 3 ahead of stage 1.
+  if (STAGED && warp <= 1) {
+    // Staged ring (two-tile CTAs, and one-tile CTAs at d = 64 without
+    // dropout): NSTAGE stages of two slots, stage t holding V of the t-th
+    // live key tile of the union and K of the next one (slots 2s and 2s + 1,
+    // s = t mod NSTAGE) on one full and one empty barrier, so that a key
+    // tile costs the issuer one load wait and one release.  K of the first
+    // tile goes to the last stage's K slot ahead of that stage's first use.
+    constexpr int NSTAGE = C::NSLOT / 2, LAST = NSTAGE - 1;
     constexpr uint32_t slot_step = C::TILE >> 4;  // descriptor units per ring slot
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------- producer
+      auto load_tile = [&](const CUtensorMap* map, int slot, uint32_t fb, int kt) {
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(s0 + C::OFF_KV + slot * C::TILE + h * C::HALF, map, fb, h * 64,
+                      cy(kt * 128), cz(kt * 128));
+      };
       bool ok = true;
       int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
       int t = 0;  // stages issued
       const int first_k = kt < p.T ? 1 : 0;
       if (first_k) {
-        mbar_expect_tx(bar(C::B_FULL + 1), C::TILE);
-        tma_load_3d(s0 + C::OFF_KV + 3 * C::TILE, &tm_k, bar(C::B_FULL + 1), 0, cy(kt * 128),
-                    cz(kt * 128));
+        mbar_expect_tx(bar(C::B_FULL + LAST), C::TILE);
+        load_tile(&tm_k, 2 * LAST + 1, bar(C::B_FULL + LAST), kt);
       }
       while (ok && kt < p.T) {
         const int nxt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt);
-        const int s = t & 1;
-        // stage t reuses the slots of stage t - 2, released by the issuer
-        // after key tile t - 2; stage 1 waits for the first S instead (slot 3)
-        if (t >= 1 &&
-            !(ok = mbar_wait(bar(C::B_EMPTY + s), ((t - 1) >> 1) & 1, ab, kSleepHintNs)))
-          break;
+        const int s = t % NSTAGE;
+        // stage t reuses the slots of stage t - NSTAGE, released by the
+        // issuer after key tile t - NSTAGE; the last stage's first use waits
+        // for the first S instead (its K slot held the first K)
+        if (s == LAST || t >= NSTAGE) {
+          const int ph = s == LAST ? t / NSTAGE : t / NSTAGE - 1;
+          if (!(ok = mbar_wait(bar(C::B_EMPTY + s), ph & 1, ab, kSleepHintNs))) break;
+        }
         const uint32_t fb = bar(C::B_FULL + s);
         mbar_expect_tx(fb, (nxt < p.T ? 2 : 1) * C::TILE);
-        tma_load_3d(s0 + C::OFF_KV + 2 * s * C::TILE, &tm_v, fb, 0, cy(kt * 128), cz(kt * 128));
-        if (nxt < p.T)
-          tma_load_3d(s0 + C::OFF_KV + (2 * s + 1) * C::TILE, &tm_k, fb, 0, cy(nxt * 128),
-                      cz(nxt * 128));
+        load_tile(&tm_v, 2 * s, fb, kt);
+        if (nxt < p.T) load_tile(&tm_k, 2 * s + 1, fb, nxt);
         ++t;
         kt = nxt;
       }
       // Drain (matters only after an abort): the last phase issued on each
-      // full barrier -- stages 0, 2, ... on barrier 0; the first K and
-      // stages 1, 3, ... on barrier 1 -- and the query tile.
-      const int nphase[2] = {(t + 1) >> 1, first_k + (t >> 1)};
-      for (int b2 = 0; b2 < 2; ++b2) {
-        if (nphase[b2] == 0) continue;
+      // full barrier (stages s, s + NSTAGE, ...; the first K too on the
+      // last one) and the query tiles.
+      for (int s = 0; s < NSTAGE; ++s) {
+        const int nph = (t > s ? (t - s - 1) / NSTAGE + 1 : 0) + (s == LAST ? first_k : 0);
+        if (nph == 0) continue;
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(bar(C::B_FULL + b2), (nphase[b2] - 1) & 1) &&
+        while (!mbar_try_wait(bar(C::B_FULL + s), (nph - 1) & 1) &&
                globaltimer() - t0 < kWaitLimitNs) {
         }
       }
@@ -390,45 +400,104 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
       // ------------------------------------------------------- MMA issuer
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
-      const uint64_t dq = sdesc_sw128(s0 + C::OFF_Q, 16, 1024);
+      const uint64_t dq0 = sdesc_sw128(s0 + C::OFF_Q, 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(s0 + C::OFF_Q + C::TILE, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(s0 + C::OFF_KV, 16, 1024);      // K operand of slot 0
       const uint64_t dv0 = sdesc_sw128(s0 + C::OFF_KV, C::HALF, 1024);  // V operand of slot 0
-      const uint32_t t_s = tmem + C::COL_S0, t_o = tmem + C::COL_O0, t_p = tmem + C::COL_P;
+      const uint32_t t_s0 = tmem + C::COL_S0, t_s1 = tmem + C::COL_S1;
+      const uint32_t t_o0 = tmem + C::COL_O0, t_o1 = tmem + C::COL_O1;
+      auto qk = [&](uint32_t t_s, uint64_t dq, int slot) {
+        if (D == 128)
+          mma_ss_kmajor_k128_h16k(t_s, dq, dk0 + (uint64_t)(slot * slot_step), id_qk, 0);
+        else
+          mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)(slot * slot_step), id_qk, 0);
+      };
+      const bool masked = p.block_mask != nullptr;
+      auto live0 = [&](int kt) {
+        return masked ? live_bit(live, 0, ufirst, kt) : (kt >= first0 && kt <= last0);
+      };
+      auto live1 = [&](int kt) {
+        if constexpr (SOLO) return false;
+        return masked ? live_bit(live, 1, ufirst, kt) : (kt >= first1 && kt <= last1);
+      };
       bool ok = mbar_wait(bar(C::B_Q), 0, ab);
       tc_fence_after();
       int kt = next_union_tile<SOLO>(p, live, ufirst, ulast, -1);
+      int ns0 = 0;  // S of query tile 0 issued (one-tile d = 64: for s_free)
       if (ok && kt < p.T) {
-        ok = mbar_wait(bar(C::B_FULL + 1), 0, ab);
+        ok = mbar_wait(bar(C::B_FULL + LAST), 0, ab);
         tc_fence_after();
         if (ok) {
-          mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)(3 * slot_step), id_qk, 0);
-          mma_commit(bar(C::B_S));
-          mma_commit(bar(C::B_EMPTY + 1));
+          if (SOLO || live0(kt)) {
+            qk(t_s0, dq0, 2 * LAST + 1);
+            mma_commit(bar(C::B_S + 0));
+            ++ns0;
+          }
+          if (live1(kt)) {
+            qk(t_s1, dq1, 2 * LAST + 1);
+            mma_commit(bar(C::B_S + 1));
+          }
+          mma_commit(bar(C::B_EMPTY + LAST));
         }
       }
+      int npv0 = 0, npv1 = 0;
       for (int j = 0; ok && kt < p.T; ++j) {
         const int nxt = next_union_tile<SOLO>(p, live, ufirst, ulast, kt);
-        const int s = j & 1;
-        // stage j is phase j / 2 of full barrier 0 (j even) or phase
-        // (j + 1) / 2 of full barrier 1 (j odd, after the first K)
-        if (!(ok = mbar_wait(bar(C::B_FULL + s), ((j + s) >> 1) & 1, ab))) break;
+        const int s = j % NSTAGE;
+        // a one-tile CTA's union is its own tiles: every tile is live
+        const bool l0 = SOLO || live0(kt), l1 = live1(kt);
+        const bool n0 = nxt < p.T && (SOLO || live0(nxt)), n1 = nxt < p.T && live1(nxt);
+        const uint64_t dv = dv0 + (uint64_t)(2 * s * slot_step);
+        // stage j is phase j / NSTAGE of its full barrier (one more on the
+        // last barrier, which first carried the first K)
+        const int ph = s == LAST ? j / NSTAGE + 1 : j / NSTAGE;
+        if (!(ok = mbar_wait(bar(C::B_FULL + s), ph & 1, ab))) break;
         tc_fence_after();
-        if (nxt < p.T) {
+        if constexpr (SEPP) {
           // the next S as soon as the softmax has read this one (P has
-          // columns of its own)
-          if (!(ok = mbar_wait(bar(C::B_SFREE), j & 1, ab))) break;
-          tc_fence_after();
-          mma_ss_kmajor_k64(t_s, dq, dk0 + (uint64_t)((2 * s + 1) * slot_step), id_qk, 0);
-          mma_commit(bar(C::B_S));
+          // columns of its own), then P . V once P is ready
+          if (n0) {
+            if (!(ok = mbar_wait(bar(C::B_SFREE), (ns0 - 1) & 1, ab))) break;
+            tc_fence_after();
+            qk(t_s0, dq0, 2 * s + 1);
+            mma_commit(bar(C::B_S + 0));
+            ++ns0;
+          }
+          if (l0) {
+            if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
+            tc_fence_after();
+            mma_ts_mn_k128(t_o0, tmem + C::COL_P, dv, id_pv, npv0 > 0);
+            mma_commit(bar(C::B_PFREE));
+            ++npv0;
+          }
+        } else {
+          // P over S: S_i of the next tile after P_i . V has read P_i
+          if (l0) {
+            if (!(ok = mbar_wait(bar(C::B_P + 0), npv0 & 1, ab))) break;
+            tc_fence_after();
+            mma_ts_mn_k128(t_o0, t_s0, dv, id_pv, npv0 > 0);
+            ++npv0;
+          }
+          if (n0) {
+            qk(t_s0, dq0, 2 * s + 1);
+            mma_commit(bar(C::B_S + 0));
+          }
+          if (l1) {
+            if (!(ok = mbar_wait(bar(C::B_P + 1), npv1 & 1, ab))) break;
+            tc_fence_after();
+            mma_ts_mn_k128(t_o1, t_s1, dv, id_pv, npv1 > 0);
+            ++npv1;
+          }
+          if (n1) {
+            qk(t_s1, dq1, 2 * s + 1);
+            mma_commit(bar(C::B_S + 1));
+          }
         }
-        if (!(ok = mbar_wait(bar(C::B_P), j & 1, ab))) break;
-        tc_fence_after();
-        mma_ts_mn_k128(t_o, t_p, dv0 + (uint64_t)(2 * s * slot_step), id_pv, j > 0);
-        mma_commit(bar(C::B_PFREE));
         mma_commit(bar(C::B_EMPTY + s));
         kt = nxt;
       }
-      mma_commit(bar(C::B_O));
+      mma_commit(bar(C::B_O + 0));
+      if constexpr (!SOLO) mma_commit(bar(C::B_O + 1));
       // Drain all issued tensor-core work before TMEM can be released.
       mma_commit(bar(C::B_DRAIN));
       const uint64_t t0 = globaltimer();
