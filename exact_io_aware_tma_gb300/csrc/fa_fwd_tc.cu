@@ -506,6 +506,8 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (unstaged: the one-tile kernel with P over S -- d = 128, or dropout --
+    // whose two slots hold one key tile's K and V, each released on its own)
     if (lane == 0) {
       int slot = 0, round = 0;
       // per-slot count of loads issued, for the final drain
@@ -549,9 +551,10 @@ __global__ void __launch_bounds__(FwdTc<D, SOLO>::THREADS, SOLO ? 2 : 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Kept lean: one thread issues every GEMM as a single instruction
-    // sequence from precomputed descriptors, so the tensor core is not left
-    // waiting on this thread's bookkeeping.
+    // (unstaged, as the producer above; the second query tile's branches are
+    // compiled out there.)  Kept lean: one thread issues every GEMM as a
+    // single instruction sequence from precomputed descriptors, so the
+    // tensor core is not left waiting on this thread's bookkeeping.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
