@@ -67,14 +67,14 @@ struct PTc {
   // B_KV[b]: K/V buffer b loaded; B_FULL/B_EMPTY: the step ring; B_S[b]:
   // S^T, dP^T of buffer b computed; B_EW[b]: P^T, dS^T of buffer b written;
   // B_DQF/B_DQE[b]: dQ^T buffer b computed / read out; B_SF[b]: dV has read
-  // P^T of S buffer b; B_DSF[b]: the products that read dS^T buffer b done;
-  // B_FIN: an item's dK, dV complete; B_DRAIN: per issuer, its last
+  // P^T of S buffer b (dS^T buffer b is free once B_DQF[b] completes: dQ^T
+  // is its last reader); B_FIN: an item's dK, dV complete; B_DRAIN: per issuer, its last
   // products done; B_ITEM[b]: item published in buffer b; B_ITEMF[b]: every
   // role done with it; B_KVF[b]: K/V buffer b free (its item's products and
   // dK/dV store done); B_ACCF: dK, dV read out of TMEM.
   static constexpr int B_KV = 0, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS, B_EW = B_S + 2,
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
-                       B_DRAIN = B_FIN + 1, B_DSF = B_DRAIN + 2, B_ITEM = B_DSF + 2,
+                       B_DRAIN = B_FIN + 1, B_ITEM = B_DRAIN + 2,
                        B_ITEMF = B_ITEM + 2, B_KVF = B_ITEMF + 2, B_ACCF = B_KVF + 2,
                        NBAR = B_ACCF + 1;
   // misc: TMEM address (+0), abort flag (+16), two PItem buffers (+64)
@@ -433,7 +433,6 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
             }
             mma_ss_mn_mn_k128(tmem + C::COL_DQ + 64 * bf, dk_mn, ds, id_q, 0);
             mma_commit(bar(C::B_DQF + bf));
-            mma_commit(bar(C::B_DSF + bf));
           }
           // dK and dV are complete once this thread's last products are (the
           // other issuer's finished before they could start), and so is
@@ -534,9 +533,10 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
         // each group overwrites only columns it has already read)
         tmem_st16(lane_base + C::COL_S + 64 * bf + qo, pk);
         // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of
-        // step s-2 (which read this buffer) have completed.
+        // step s-2 (which read this buffer) have completed: the commit after
+        // dQ^T, the last of them, covers both.
         if (s >= 2) {
-          if (!(ok = mbar_wait(bar(C::B_DSF + bf), ((s - 2) >> 1) & 1, ab))) break;
+          if (!(ok = mbar_wait(bar(C::B_DQF + bf), ((s - 2) >> 1) & 1, ab))) break;
         }
         uint8_t* dsb = smem + C::OFF_DS + bf * C::DS + r * 128;
 #pragma unroll

@@ -86,6 +86,7 @@ struct BwdTc {
   static constexpr int DS = 128 * BQ * 2;             // dS^T [128 keys][64 q] bf16, x2
   static constexpr int OFF_BAR = OFF_DS + 2 * DS;
   // B_DSF[b]: the gradient GEMMs that read dS^T buffer b have completed
+  // (d = 128; at d = 64 dQ^T is their last and B_DQF[b] says so)
   static constexpr int B_KV = 0, B_FULL = 1, B_EMPTY = 1 + NS, B_S = 1 + 2 * NS, B_EW = B_S + 2,
                        B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
                        B_DRAIN = B_FIN + 1, B_DSF = B_DRAIN + 2, NBAR = B_DSF + 2;
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
             mma_ss_mn_mn_k128(tmem + C::COL_DQ + 64 * bf, dk_mn, ds, id_q, 0);
             mma_commit(bar(C::B_DQF + bf));
           }
-          mma_commit(bar(C::B_DSF + bf));
+          if constexpr (!C::SEPQ) mma_commit(bar(C::B_DSF + bf));
         }
         // dK and dV are complete once this thread's last MMAs are (the other
         // issuer's work for the last step finished before it could start)
@@ -525,9 +526,11 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
       else
         tmem_st16(lane_base + C::COL_S + 64 * bf + qo, pk);
       // dS^T row r into the 128-byte-swizzled buffer bf, once dK / dQ^T of
-      // step i-2 (which read this buffer) have completed.
+      // step i-2 (which read this buffer) have completed (at d = 64 the
+      // commit after dQ^T, the last of them, covers both).
       if (i >= 2) {
-        if (!(ok = mbar_wait(bar(C::B_DSF + bf), ((i - 2) >> 1) & 1, ab, crit_hint))) break;
+        const uint32_t fb = bar((C::SEPQ ? C::B_DQF : C::B_DSF) + bf);
+        if (!(ok = mbar_wait(fb, ((i - 2) >> 1) & 1, ab, crit_hint))) break;
       }
       uint8_t* dsb = smem + C::OFF_DS + bf * C::DS + r * 128;
 #pragma unroll
