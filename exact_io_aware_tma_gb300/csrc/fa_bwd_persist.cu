@@ -64,16 +64,17 @@ struct PTc {
   static constexpr int OFF_DS = (OFF_VEC + NS * 512 + 1023) / 1024 * 1024;
   static constexpr int DS = 128 * BQ * 2;        // dS^T [128 keys][64 q] bf16, x2
   static constexpr int OFF_BAR = OFF_DS + 2 * DS;
-  // B_KV[b]: K/V buffer b loaded; B_FULL/B_EMPTY: the step ring; B_S[b]:
-  // S^T, dP^T of buffer b computed; B_EW[b]: P^T, dS^T of buffer b written;
-  // B_DQF/B_DQE[b]: dQ^T buffer b computed / read out; B_SF[b]: dV has read
-  // P^T of S buffer b (dS^T buffer b is free once B_DQF[b] completes: dQ^T
-  // is its last reader); B_FIN: an item's dK, dV complete; B_DRAIN: per issuer, its last
+  // B_KV[b]: K/V buffer b loaded; B_FULL/B_EMPTY: the step ring (a step's
+  // release, after its dK, also says that its dV has read P^T out of S
+  // buffer b); B_S[b]: S^T, dP^T of buffer b computed; B_EW[b]: P^T, dS^T of
+  // buffer b written; B_DQF/B_DQE[b]: dQ^T buffer b computed / read out
+  // (dS^T buffer b is free once B_DQF[b] completes: dQ^T is its last
+  // reader); B_FIN: an item's dK, dV complete; B_DRAIN: per issuer, its last
   // products done; B_ITEM[b]: item published in buffer b; B_ITEMF[b]: every
   // role done with it; B_KVF[b]: K/V buffer b free (its item's products and
   // dK/dV store done); B_ACCF: dK, dV read out of TMEM.
   static constexpr int B_KV = 0, B_FULL = 2, B_EMPTY = 2 + NS, B_S = 2 + 2 * NS, B_EW = B_S + 2,
-                       B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_SF = B_DQE + 2, B_FIN = B_SF + 2,
+                       B_DQF = B_EW + 2, B_DQE = B_DQF + 2, B_FIN = B_DQE + 2,
                        B_DRAIN = B_FIN + 1, B_ITEM = B_DRAIN + 2,
                        B_ITEMF = B_ITEM + 2, B_KVF = B_ITEMF + 2, B_ACCF = B_KVF + 2,
                        NBAR = B_ACCF + 1;
@@ -367,7 +368,8 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
     // ------------------------------------------------------------ MMA issuers
     //   warp 1: S^T(j), dP^T(j) into buffer j % 2 (owns TMEM);
     //   warp 2: dV(i), dK(i), dQ^T(i) into dQ[i % 2].
-    // S^T(j) waits until dV(j-2) has read P^T(j-2) from the same columns;
+    // S^T(j) waits until dV(j-2) has read P^T(j-2) from the same columns
+    // (the release of step j-2's stage, committed after its dK, says so);
     // dQ^T(i) until the dQ warps have read dQ^T(i-2) out.  j, i count the
     // CTA's steps (across items); dV and dK accumulate from each item's
     // first step.
@@ -400,7 +402,9 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
             const int bf = j & 1;
             const uint64_t sq = dst_k + (uint64_t)((j % C::NS) * st_step);
             if (!(ok = mbar_wait(bar(C::B_FULL + j % C::NS), (j / C::NS) & 1, ab))) break;
-            if (j >= 2 && !(ok = mbar_wait(bar(C::B_SF + bf), ((j - 2) >> 1) & 1, ab))) break;
+            if (j >= 2 &&
+                !(ok = mbar_wait(bar(C::B_EMPTY + (j - 2) % C::NS), ((j - 2) / C::NS) & 1, ab)))
+              break;
             tc_fence_after();
             mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
             mma_ss_kmajor_k64_a16k_b8k(tmem + C::COL_DP + 64 * bf, dv_k, sq + qb_step, id_s, 0);
@@ -422,7 +426,6 @@ __global__ void __launch_bounds__(PTc::THREADS, 1)
             // dV += P^T dO   (P^T: bf16 in TMEM over S[bf], the two groups'
             // halves 32 columns apart; dO as MN-major B)
             mma_ts_mn_k64_gap32(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, ii > 0);
-            mma_commit(bar(C::B_SF + bf));
             // dK += dS^T Q
             mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, ii > 0);
             mma_commit(bar(C::B_EMPTY + i % C::NS));
