@@ -317,8 +317,9 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
     //   warp 2: d = 64: dV(i), dK(i), dQ^T(i) into dQ[i % 2];
     //           d = 128: dQ^T(i) over dP[i % 2], dV(i), dK(i).
     // S^T(j) waits until dV(j-2) has read P^T(j-2) from the same columns
-    // (s_free); at d = 128 dP^T(j) waits until the dQ warps have read
-    // dQ^T(j-2) out, at d = 64 dQ^T(i) waits for that instead.
+    // (s_free at d = 128; at d = 64 the release of step j-2's Q, dO stage,
+    // committed after its dK); at d = 128 dP^T(j) waits until the dQ warps
+    // have read dQ^T(j-2) out, at d = 64 dQ^T(i) waits for that instead.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, C::BQ, false, false);
       constexpr uint32_t id_kv = idesc_bf16(128, D, false, true);
@@ -342,7 +343,13 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
           const int bf = j & 1;
           const uint64_t sq = dst_k + (uint64_t)((j % C::NS) * st_step);
           if (!(ok = mbar_wait(bar(C::B_FULL + j % C::NS), (j / C::NS) & 1, ab, crit_hint))) break;
-          if (j >= 2 && !(ok = mbar_wait(bar(C::B_SF + bf), ((j - 2) >> 1) & 1, ab, crit_hint))) break;
+          // d = 64: the release of step j-2's Q, dO stage (after its dK,
+          // which follows its dV) says that dV has read P^T(j-2)
+          if (j >= 2 && !(ok = mbar_wait(C::SEPQ ? bar(C::B_EMPTY + (j - 2) % C::NS)
+                                                 : bar(C::B_SF + bf),
+                                         C::SEPQ ? ((j - 2) / C::NS) & 1 : ((j - 2) >> 1) & 1,
+                                         ab, crit_hint)))
+            break;
           tc_fence_after();
           if (D == 128)
             mma_ss_kmajor_k128_a16k_b8k(tmem + C::COL_S + 64 * bf, dk_k, sq, id_s, 0);
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(BwdEw<D, DROP>::THREADS, 1)
             mma_ts_mn_k64_gap32(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
           else
             mma_ts_mn_k64(t_dv, tmem + C::COL_S + 64 * bf, sq_mn + qb_step, id_kv, i > 0);
-          mma_commit(bar(C::B_SF + bf));
+          if constexpr (!C::SEPQ) mma_commit(bar(C::B_SF + bf));
           // dK += dS^T Q
           mma_ss_kmajor_mn_k64(t_dk, ds, sq_mn, id_kv, i > 0);
           mma_commit(bar(C::B_EMPTY + i % C::NS));
